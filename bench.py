@@ -1,0 +1,350 @@
+"""Benchmark: causal attention fwd+bwd TFLOP/s (bf16) at L=128K on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 7b_128k] [--impl ours|reference]
+
+A step is one pass of the whole hot path over the workload: forward tile
+kernel, LSE merge of the re-split edge chunks, backward preprocess, backward
+key-tile kernel, dQ finalize. `value` counts algorithmic FLOPs only: 14*D per
+visible (query, key) pair (2 forward GEMMs, 5 backward GEMMs). Inputs (1 GiB
+per tensor) are far larger than the 129 MB L2, so no flush is needed between
+steps. Under torchrun every rank runs its own replica of the workload (the
+heads are independent; no data-path collective) and rank 0 prints one JSON
+line with the whole-job throughput (weak scaling).
+
+--impl reference times the float64 CPU oracle on the same workload, metric
+and unit, each step a bounded sample (a causal prefix of one head).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+METRIC = "causal attn fwd+bwd TFLOP/s (bf16) at L=128K, % of GB300 dense BF16 peak"
+CPU_SAMPLE_TOKENS = 40960     # causal prefix of one head timed on the host cores
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def causal_pairs_total(w, chunks):
+    from chunked_causal_attention_gb300.workloads import Workload  # noqa: F401
+    if w.packed:
+        lens = w.doc_lens
+        per = sum(n * (n + 1) // 2 for n in lens)
+    else:
+        per = w.L * (w.L + 1) // 2
+    return per * w.B * w.H
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, path=None):
+        self.proc = None
+        self.path = path
+        self.lines = []
+        self.bus = None
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(device_index)
+            self.bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus:
+            cmd += ["-i", self.bus]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+        if self.path:
+            with open(self.path, "w") as f:
+                f.write(self.QUERY + "\n" + "\n".join(self.lines) + "\n")
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle arm
+def time_oracle_sample(w, tokens, seed):
+    """Oracle fwd+bwd (float64, host cores) on a causal prefix of one head."""
+    import numpy as np
+    from chunked_causal_attention_gb300.workloads import make_inputs
+    from oracle import attention as A
+    D = w.D
+    q, k, v, do = (x[0, 0].float().numpy() for x in make_inputs(1, 1, tokens, D, seed=seed))
+    t0 = time.perf_counter()
+    A.backward(q, k, v, do, w.scale, None, row_block=1024)
+    dt = time.perf_counter() - t0
+    pairs = tokens * (tokens + 1) // 2
+    return 14 * D * pairs / dt / 1e12, dt
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from chunked_causal_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    for i in range(args.warmup):
+        time_oracle_sample(w, CPU_SAMPLE_TOKENS // 4, 7000 + i)
+    vals, secs = [], []
+    for i in range(args.steps):
+        v, dt = time_oracle_sample(w, CPU_SAMPLE_TOKENS, 8000 + i)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.median(vals)
+    sample = (f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of {CPU_SAMPLE_TOKENS} tokens "
+              f"of one head (D={w.D}) per step; TFLOP/s = 14*D*pairs/time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, args),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args):
+    return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "tokens": w.L, "plan_chunks": w.N,
+            "plan_mode": ["uniform", "flops", "flops_resplit_edges"][w.mode], "packed": w.packed,
+            "l2": "inputs larger than L2 (1 GiB per tensor); no flush", "parallelism": f"replicas x{args.gpus}"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import chunked_causal_attention_gb300 as cca
+    from chunked_causal_attention_gb300.workloads import WORKLOADS, workload_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    w = WORKLOADS[args.workload]
+    if w.packed:
+        chunks = cca.attn_plan_varlen(w.cu_seqlens(), w.max_chunk_tokens, w.mode)
+    else:
+        chunks = cca.attn_plan(w.L, w.N, w.mode)
+    q, k, v, do = workload_inputs(w, device=dev)
+    shape = cca.shape_of(q, w.scale, w.packed)
+    o = torch.empty_like(q)
+    lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_f = cca.workspace(shape, chunks, 0, dev)
+    ws_b = cca.workspace(shape, chunks, 1, dev)
+    stream = torch.cuda.current_stream(dev)
+    has_merge = any(c[3] for c in chunks)
+    stages = ["fwd_tiles", "fwd_merge", "bwd_prep", "bwd_tiles", "bwd_dq"]
+    launches_per_step = 4 + (1 if has_merge else 0)
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        cca.attn_fwd_tiles(q, k, v, chunks, shape, o, lse, ws_f, stream)
+        mark(1)
+        cca.attn_fwd_merge(chunks, shape, o, lse, ws_f, stream)
+        mark(2)
+        cca.attn_bwd_prep(o, do, chunks, shape, ws_b, stream)
+        mark(3)
+        cca.attn_bwd_tiles(q, k, v, lse, do, chunks, shape, dk, dv, ws_b, stream)
+        mark(4)
+        cca.attn_bwd_dq(chunks, shape, dq, ws_b, stream)
+        mark(5)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = cca.attn_status(ws_f, stream) or cca.attn_status(ws_b, stream)
+    if st:
+        raise RuntimeError(f"device status after warm-up: {cca.strerror(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, s in enumerate(stages)}
+    st = cca.attn_status(ws_f, stream) or cca.attn_status(ws_b, stream)
+    if st:
+        raise RuntimeError(f"device status after timed steps: {cca.strerror(st)}")
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    pairs = causal_pairs_total(w, chunks)
+    flops_fwd = 4 * w.D * pairs
+    flops_bwd = 10 * w.D * pairs
+    flops_step = flops_fwd + flops_bwd
+    ms_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    e2e_steps = max(1, min(args.steps, 3))
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    q2, k2, v2, do2 = (torch.empty_like(x) for x in (q, k, v, do))
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
+            d_.copy_(h_, non_blocking=True)
+        cca.attn_fwd(q2, k2, v2, chunks, shape, o2, lse2, ws_f, stream)
+        cca.attn_bwd(q2, k2, v2, o2, lse2, do2, chunks, shape, dq_, dk_, dv_, ws_b, stream)
+        for h_, d_ in ((ho, o2), (hlse, lse2), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            h_.copy_(d_, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    nbytes = lambda x: x.numel() * x.element_size()
+    h2d = sum(nbytes(x) for x in (q, k, v, do))
+    d2h = sum(nbytes(x) for x in (o, lse, dq, dk, dv))
+    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    dom = "bwd_tiles"
+    dom_ms = stage_ms[dom]
+    achieved = flops_bwd / (dom_ms * 1e-3) / 1e12
+    peak_sus = peaks["bf16_tflops_sustained"]
+    peak_burst = peaks["bf16_tflops"]
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, args),
+            "pct_of_peak": {"burst": 100 * value / world / peak_burst, "sustained": 100 * value / world / peak_sus,
+                            "peak_source": peak_src},
+            "fwd_tflops": flops_fwd / ((stage_ms["fwd_tiles"] + stage_ms["fwd_merge"]) * 1e-3) / 1e12,
+            "bwd_tflops": flops_bwd / ((stage_ms["bwd_prep"] + stage_ms["bwd_tiles"] + stage_ms["bwd_dq"]) * 1e-3)
+                          / 1e12,
+            "stage_ms": stage_ms,
+            "roofline": {"kernel": "bwd key-tile kernel (attn_bwd_tiles)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
+                         "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                         "frac_of_burst": achieved / peak_burst, "traffic": None},
+            "gpu_launches": launches_per_step * args.steps,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v_cpu, dt = time_oracle_sample(w, CPU_SAMPLE_TOKENS, 9000)
+            line["cpu_baseline"] = {
+                "value": v_cpu, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                "sample": f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of {CPU_SAMPLE_TOKENS} "
+                          f"tokens of one head, {dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="7b_128k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,55 @@
+"""Chunked causal self-attention for GB300 (sm_103a).
+
+The compute lives in libattn.so (C ABI in include/attn.h, CUDA kernels in
+csrc/); this package is its thin binding. PyTorch provides device memory and
+streams only. ``forward`` / ``backward`` allocate outputs and the workspace
+with torch and call the library; the ``attn_*`` functions mirror the C entry
+points one to one.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+from ._lib import (AttnError, EXPORTS, PLAN_FLOPS, PLAN_FLOPS_RESPLIT_EDGES, PLAN_UNIFORM, attn_bwd,
+                   attn_bwd_dq, attn_bwd_prep, attn_bwd_tiles, attn_fwd, attn_fwd_merge, attn_fwd_tiles,
+                   attn_plan, attn_plan_varlen, attn_shape, attn_status, attn_workspace_size, lib, make_shape,
+                   shape_of, strerror, version)
+
+__all__ = ["AttnError", "EXPORTS", "PLAN_UNIFORM", "PLAN_FLOPS", "PLAN_FLOPS_RESPLIT_EDGES", "attn_plan",
+           "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles", "attn_fwd_merge", "attn_bwd",
+           "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_status", "attn_shape", "make_shape",
+           "shape_of", "workspace", "forward", "backward", "lib", "strerror", "version"]
+
+
+def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda"):
+    """A uint8 device buffer of the size the library asks for (pass 0 forward,
+    1 backward), with its 256-byte status header zeroed."""
+    import torch
+    n = attn_workspace_size(shape, chunks, pass_)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def forward(q, k, v, chunks: Sequence, scale: Optional[float] = None, packed: bool = False, ws=None, stream=None):
+    """(o, lse) of chunked causal attention; q, k, v bf16 [B, H, L, D] (or packed [T, H, D])."""
+    import torch
+    shape = shape_of(q, scale, packed)
+    o = torch.empty_like(q)
+    lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, chunks, 0, q.device)
+    attn_fwd(q, k, v, chunks, shape, o, lse, ws, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = None, packed: bool = False,
+             ws=None, stream=None):
+    """(dq, dk, dv) for upstream gradient dout, given the forward's o and lse."""
+    import torch
+    shape = shape_of(q, scale, packed)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if ws is None:
+        ws = workspace(shape, chunks, 1, q.device)
+    attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream)
+    return dq, dk, dv

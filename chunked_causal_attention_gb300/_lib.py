@@ -1,0 +1,218 @@
+"""ctypes binding of libattn (include/attn.h): argument marshalling only.
+
+Every function here converts Python/torch arguments to the C ABI's plain
+pointers and sizes and calls the entry point of the same name. All compute
+runs in the library's CUDA kernels; there is no Python or CPU fallback: if
+libattn.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_E_INVAL", 2: "ATTN_E_ALIGN", 3: "ATTN_E_UNSUPPORTED",
+                4: "ATTN_E_WORKSPACE", 5: "ATTN_E_CUDA", 6: "ATTN_E_TIMEOUT", 7: "ATTN_E_BOUNDS",
+                8: "ATTN_E_CAPACITY"}
+
+PLAN_UNIFORM = 0
+PLAN_FLOPS = 1
+PLAN_FLOPS_RESPLIT_EDGES = 2
+
+# Every symbol include/attn.h declares.
+EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
+           "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
+           "attn_status", "attn_strerror", "attn_version")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({strerror(status)})")
+
+
+class attn_chunk(ctypes.Structure):
+    _fields_ = [("q_begin", ctypes.c_int32), ("q_end", ctypes.c_int32),
+                ("ctx_begin", ctypes.c_int32), ("kv_split", ctypes.c_int32)]
+
+
+class attn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("sb", ctypes.c_int64), ("st", ctypes.c_int64), ("sh", ctypes.c_int64),
+                ("scale", ctypes.c_float)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_VP = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_CP = ctypes.POINTER(attn_chunk)
+_SP = ctypes.POINTER(attn_shape)
+_SIG = {
+    "attn_plan": ([_I64, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "attn_plan_varlen": ([ctypes.POINTER(_I64), _I32, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "attn_workspace_size": ([_SP, _CP, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "attn_fwd": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_fwd_tiles": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_fwd_merge": ([_CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
+                 ctypes.c_int),
+    "attn_bwd_prep": ([_VP, _VP, _CP, _I32, _SP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_bwd_tiles": ([_VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
+                       ctypes.c_int),
+    "attn_bwd_dq": ([_CP, _I32, _SP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_status": ([_VP, _VP], ctypes.c_int),
+    "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "attn_version": ([], ctypes.c_char_p),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so (built in-tree by chunked_causal_attention_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libattn.so not built ({LIB_PATH}); run `python -m "
+                               "chunked_causal_attention_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIG.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().attn_strerror(status).decode()
+
+
+def version() -> str:
+    return lib().attn_version().decode()
+
+
+def _check(fn: str, st: int) -> None:
+    if st != ATTN_OK:
+        raise AttnError(fn, st)
+
+
+def chunk_array(chunks: Sequence[Sequence[int]]):
+    arr = (attn_chunk * max(1, len(chunks)))()
+    for i, c in enumerate(chunks):
+        arr[i] = attn_chunk(*[int(x) for x in c])
+    return arr, len(chunks)
+
+
+# ------------------------------------------------------------------ planning
+
+def attn_plan(L: int, N: int, mode: int) -> List[Tuple[int, int, int, int]]:
+    out = (attn_chunk * max(1, N))()
+    n = _I32(0)
+    _check("attn_plan", lib().attn_plan(L, N, mode, out, N, ctypes.byref(n)))
+    return [(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[:n.value]]
+
+
+def attn_plan_varlen(cu_seqlens: Sequence[int], max_chunk_tokens: int, mode: int):
+    nd = len(cu_seqlens) - 1
+    cu = (_I64 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    n = _I32(0)
+    cap = 16
+    while True:
+        out = (attn_chunk * cap)()
+        st = lib().attn_plan_varlen(cu, nd, max_chunk_tokens, mode, out, cap, ctypes.byref(n))
+        if st == 8 and n.value > cap:       # ATTN_E_CAPACITY reports the needed count
+            cap = n.value
+            continue
+        _check("attn_plan_varlen", st)
+        return [(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[:n.value]]
+
+
+# ------------------------------------------------------------------ shapes
+
+def make_shape(B, H, T, D, sb, st, sh, scale) -> attn_shape:
+    return attn_shape(B, H, T, D, sb, st, sh, float(scale))
+
+
+def shape_of(x, scale: Optional[float] = None, packed: bool = False) -> attn_shape:
+    """attn_shape of a torch tensor: dense [B, H, L, D] or packed [T, H, D]."""
+    D = x.shape[-1]
+    sc = (1.0 / D ** 0.5) if scale is None else scale
+    if packed:
+        T, H, _ = x.shape
+        return make_shape(1, H, T, D, x.stride(0) * T, x.stride(0), x.stride(1), sc)
+    B, H, L, _ = x.shape
+    return make_shape(B, H, L, D, x.stride(0), x.stride(2), x.stride(1), sc)
+
+
+def attn_workspace_size(shape: attn_shape, chunks, pass_: int) -> int:
+    arr, n = chunk_array(chunks)
+    out = ctypes.c_size_t(0)
+    _check("attn_workspace_size", lib().attn_workspace_size(ctypes.byref(shape), arr, n, pass_, ctypes.byref(out)))
+    return out.value
+
+
+# ------------------------------------------------------------------ compute
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def attn_fwd(q, k, v, chunks, shape, o, lse, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape), _ptr(o), _ptr(lse),
+                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_fwd_tiles(q, k, v, chunks, shape, o, lse, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_fwd_tiles", lib().attn_fwd_tiles(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape), _ptr(o),
+                                                  _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+                                                  _stream(stream)))
+
+
+def attn_fwd_merge(chunks, shape, o, lse, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_fwd_merge", lib().attn_fwd_merge(arr, n, ctypes.byref(shape), _ptr(o), _ptr(lse), _ptr(ws),
+                                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_bwd", lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr, n,
+                                      ctypes.byref(shape), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_bwd_prep(o, dout, chunks, shape, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_bwd_prep", lib().attn_bwd_prep(_ptr(o), _ptr(dout), arr, n, ctypes.byref(shape), _ptr(ws),
+                                                ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_bwd_tiles(q, k, v, lse, dout, chunks, shape, dk, dv, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_bwd_tiles", lib().attn_bwd_tiles(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dout), arr, n,
+                                                  ctypes.byref(shape), _ptr(dk), _ptr(dv), _ptr(ws),
+                                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
+    arr, n = chunk_array(chunks)
+    _check("attn_bwd_dq", lib().attn_bwd_dq(arr, n, ctypes.byref(shape), _ptr(dq), _ptr(ws),
+                                            ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_status(ws, stream=None) -> int:
+    return lib().attn_status(_ptr(ws), _stream(stream))

@@ -1,0 +1,349 @@
+// C-ABI layer of libattn: argument validation, workspace layout, work lists,
+// kernel launches and status read-back. No device memory is allocated here.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "attn_internal.h"
+
+using namespace attn;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_shape(const attn_shape* s, Geom* g) {
+    if (!s) return ATTN_E_INVAL;
+    if (s->B <= 0 || s->H <= 0 || s->T <= 0 || s->D <= 0) return ATTN_E_INVAL;
+    if (s->T > INT32_MAX || s->B > INT32_MAX || s->H > INT32_MAX) return ATTN_E_INVAL;
+    if ((int64_t)s->B * s->H > (1ll << 24)) return ATTN_E_INVAL;
+    if (s->D != 64 && s->D != 128) return ATTN_E_UNSUPPORTED;
+    if (s->sb <= 0 || s->st <= 0 || s->sh <= 0) return ATTN_E_INVAL;
+    if (!std::isfinite(s->scale)) return ATTN_E_INVAL;
+    if ((s->sb % 8) || (s->st % 8) || (s->sh % 8)) return ATTN_E_ALIGN;
+    g->B = (int32_t)s->B; g->H = (int32_t)s->H; g->T = (int32_t)s->T; g->D = (int32_t)s->D;
+    g->sb = s->sb; g->st = s->st; g->sh = s->sh; g->scale = s->scale;
+    return ATTN_OK;
+}
+
+// Forward chunk rules: sorted by q_begin, disjoint, 0 <= ctx <= qb < qe <= T,
+// kv_split == 0 or ctx < m < qe.
+int check_chunks_fwd(const attn_chunk* c, int32_t n, int32_t T) {
+    if (n < 0 || (n > 0 && !c)) return ATTN_E_INVAL;
+    for (int32_t i = 0; i < n; ++i) {
+        const attn_chunk& x = c[i];
+        if (!(0 <= x.ctx_begin && x.ctx_begin <= x.q_begin && x.q_begin < x.q_end && x.q_end <= T))
+            return ATTN_E_INVAL;
+        if (x.kv_split != 0 && !(x.ctx_begin < x.kv_split && x.kv_split < x.q_end)) return ATTN_E_INVAL;
+        if (i > 0 && c[i - 1].q_end > x.q_begin) return ATTN_E_INVAL;
+    }
+    return ATTN_OK;
+}
+
+// Backward additionally needs a partition of [0, T) into documents: chunks
+// contiguous from 0 to T; a chunk either continues the previous chunk's
+// document (same ctx_begin) or starts a new one (ctx_begin == q_begin).
+int check_chunks_bwd(const attn_chunk* c, int32_t n, int32_t T) {
+    int st = check_chunks_fwd(c, n, T);
+    if (st) return st;
+    if (n <= 0) return ATTN_E_INVAL;
+    if (c[0].q_begin != 0 || c[n - 1].q_end != T) return ATTN_E_INVAL;
+    for (int32_t i = 0; i < n; ++i) {
+        if (i > 0 && c[i - 1].q_end != c[i].q_begin) return ATTN_E_INVAL;
+        bool cont = i > 0 && c[i].ctx_begin == c[i - 1].ctx_begin;
+        if (!cont && c[i].ctx_begin != c[i].q_begin) return ATTN_E_INVAL;
+    }
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- forward layout
+struct FwdLayout {
+    std::vector<FwdItem> items;
+    std::vector<MergeSeg> segs;
+    size_t off_items, off_segs, off_parts, bytes;
+    int64_t merge_work;
+};
+
+void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
+    const int64_t BH = (int64_t)g.B * g.H;
+    L.items.clear();
+    L.segs.clear();
+    int64_t part_floats = 0;   // running float offset inside the partial region
+    L.merge_work = 0;
+    struct Pending { size_t seg; };
+    for (int32_t ci = 0; ci < n; ++ci) {
+        const attn_chunk& x = c[ci];
+        const int32_t qb = x.q_begin, qe = x.q_end, cb = x.ctx_begin, m = x.kv_split;
+        int32_t pr0 = qe;  // first row that needs partials
+        int64_t off_a = -1, off_b = -1;
+        int32_t R = 0;
+        if (m) {
+            pr0 = m > qb ? qb + kTile * ((m - qb) / kTile) : qb;
+            R = qe - pr0;
+            int64_t blk = (int64_t)round_up((size_t)(BH * R * g.D + BH * R), 64);
+            off_a = part_floats;
+            off_b = part_floats + blk;
+            part_floats += 2 * blk;
+            MergeSeg s;
+            s.row0 = pr0; s.R = R; s.off_a = off_a; s.off_b = off_b; s.work0 = L.merge_work;
+            L.merge_work += (int64_t)R * BH;
+            L.segs.push_back(s);
+        }
+        for (int32_t r0 = qb; r0 < qe; r0 += kTile) {
+            int32_t r1 = std::min(r0 + kTile, qe);
+            if (!m || r1 <= m || r0 < pr0) {
+                L.items.push_back(FwdItem{r0, r1, cb, r1, -1, 0, 0});
+            } else {
+                L.items.push_back(FwdItem{r0, r1, cb, std::min(m, r1), off_a, pr0, R});
+                L.items.push_back(FwdItem{r0, r1, m, r1, off_b, pr0, R});
+            }
+        }
+    }
+    // heaviest first (longest key range), stable for determinism
+    std::stable_sort(L.items.begin(), L.items.end(), [](const FwdItem& a, const FwdItem& b) {
+        return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
+    });
+    L.off_items = kHeaderBytes;
+    L.off_segs = L.off_items + round_up(L.items.size() * sizeof(FwdItem), kAlign);
+    L.off_parts = L.off_segs + round_up(L.segs.size() * sizeof(MergeSeg), kAlign);
+    L.bytes = L.off_parts + round_up((size_t)part_floats * sizeof(float), kAlign);
+}
+
+// --------------------------------------------------------------- backward layout
+struct BwdLayout {
+    std::vector<BwdItem> items;
+    size_t off_items, off_delta, off_dq, bytes;
+};
+
+void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
+    const int64_t BH = (int64_t)g.B * g.H;
+    L.items.clear();
+    int32_t i = 0;
+    while (i < n) {
+        int32_t s = c[i].ctx_begin, e = c[i].q_end;
+        int32_t j = i + 1;
+        while (j < n && c[j].ctx_begin == s) { e = c[j].q_end; ++j; }
+        for (int32_t j0 = s; j0 < e; j0 += kTile)
+            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, e), e, s});
+        i = j;
+    }
+    std::stable_sort(L.items.begin(), L.items.end(), [](const BwdItem& a, const BwdItem& b) {
+        return (a.q_end - a.j0) > (b.q_end - b.j0);
+    });
+    L.off_items = kHeaderBytes;
+    L.off_delta = L.off_items + round_up(L.items.size() * sizeof(BwdItem), kAlign);
+    L.off_dq = L.off_delta + round_up((size_t)BH * g.T * sizeof(float), kAlign);
+    L.bytes = L.off_dq + round_up((size_t)BH * g.T * g.D * sizeof(float), kAlign);
+}
+
+int upload(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+    if (!bytes) return ATTN_OK;
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess ? ATTN_OK : ATTN_E_CUDA;
+}
+
+int reset_header(void* ws, cudaStream_t s) {
+    return cudaMemsetAsync(ws, 0, kHeaderBytes, s) == cudaSuccess ? ATTN_OK : ATTN_E_CUDA;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_E_CUDA; }
+
+int check_ws(void* ws, size_t have, size_t need) {
+    if (!ws || have < need) return ATTN_E_WORKSPACE;
+    if (((uintptr_t)ws & (kAlign - 1)) != 0) return ATTN_E_ALIGN;
+    return ATTN_OK;
+}
+
+constexpr int32_t kGroup = 8;
+
+int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* chunks, int32_t n,
+               const attn_shape* shape, void* o, float* lse, void* ws, size_t ws_bytes,
+               cudaStream_t s, bool do_tiles, bool do_merge) {
+    Geom g;
+    int st = check_shape(shape, &g);
+    if (st) return st;
+    if ((st = check_chunks_fwd(chunks, n, g.T))) return st;
+    if (!o || !lse || (do_tiles && (!q || !k || !v))) return ATTN_E_INVAL;
+    if ((do_tiles && (!aligned16(q) || !aligned16(k) || !aligned16(v))) || !aligned16(o) ||
+        !aligned16(lse))
+        return ATTN_E_ALIGN;
+    FwdLayout L;
+    fwd_layout(g, chunks, n, L);
+    if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
+    uint8_t* w = (uint8_t*)ws;
+    float* ws_f = (float*)(w + L.off_parts);
+    if (do_tiles) {
+        if ((st = reset_header(ws, s))) return st;
+        if (!L.items.empty()) {
+            if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(FwdItem), s))) return st;
+            FwdArgs a;
+            a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.ws_f = ws_f;
+            a.status = (uint32_t*)ws;
+            a.items = (const FwdItem*)(w + L.off_items);
+            a.n_items = (int32_t)L.items.size();
+            a.group = kGroup;
+            a.g = g;
+            if ((st = launched(launch_fwd_tiles(a, s)))) return st;
+        }
+    }
+    if (do_merge && !L.segs.empty()) {
+        if ((st = upload(w + L.off_segs, L.segs.data(), L.segs.size() * sizeof(MergeSeg), s))) return st;
+        MergeArgs a;
+        a.o = o; a.lse = lse; a.ws_f = ws_f;
+        a.segs = (const MergeSeg*)(w + L.off_segs);
+        a.n_segs = (int32_t)L.segs.size();
+        a.total_work = L.merge_work;
+        a.g = g;
+        if ((st = launched(launch_fwd_merge(a, s)))) return st;
+    }
+    return ATTN_OK;
+}
+
+enum BwdStage { kPrep = 1, kTiles = 2, kDq = 4 };
+
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+               void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t s, int stages) {
+    Geom g;
+    int st = check_shape(shape, &g);
+    if (st) return st;
+    if ((st = check_chunks_bwd(chunks, n, g.T))) return st;
+    if ((stages & kPrep) && (!o || !dout)) return ATTN_E_INVAL;
+    if ((stages & kTiles) && (!q || !k || !v || !lse || !dout || !dk || !dv)) return ATTN_E_INVAL;
+    if ((stages & kDq) && !dq) return ATTN_E_INVAL;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return ATTN_E_ALIGN;
+    BwdLayout L;
+    bwd_layout(g, chunks, n, L);
+    if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
+    uint8_t* w = (uint8_t*)ws;
+    float* delta = (float*)(w + L.off_delta);
+    float* dq_acc = (float*)(w + L.off_dq);
+    if (stages & kPrep) {
+        if ((st = reset_header(ws, s))) return st;
+        PrepArgs a{o, dout, delta, dq_acc, g};
+        if ((st = launched(launch_bwd_prep(a, s)))) return st;
+    }
+    if (stages & kTiles) {
+        if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) return st;
+        BwdArgs a;
+        a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
+        a.dk = dk; a.dv = dv; a.dq_acc = dq_acc; a.status = (uint32_t*)ws;
+        a.items = (const BwdItem*)(w + L.off_items);
+        a.n_items = (int32_t)L.items.size();
+        a.group = kGroup;
+        a.g = g;
+        if ((st = launched(launch_bwd_tiles(a, s)))) return st;
+    }
+    if (stages & kDq) {
+        DqArgs a{dq_acc, dq, g};
+        if ((st = launched(launch_bwd_dq(a, s)))) return st;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32_t n, int32_t pass,
+                        size_t* bytes) {
+    if (!bytes) return ATTN_E_INVAL;
+    Geom g;
+    int st = check_shape(shape, &g);
+    if (st) return st;
+    if (pass == 0) {
+        if ((st = check_chunks_fwd(chunks, n, g.T))) return st;
+        FwdLayout L;
+        fwd_layout(g, chunks, n, L);
+        *bytes = L.bytes;
+    } else if (pass == 1) {
+        if ((st = check_chunks_bwd(chunks, n, g.T))) return st;
+        BwdLayout L;
+        bwd_layout(g, chunks, n, L);
+        *bytes = L.bytes;
+    } else {
+        return ATTN_E_INVAL;
+    }
+    return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, const attn_chunk* chunks, int32_t n,
+             const attn_shape* shape, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    return fwd_common(q, k, v, chunks, n, shape, o, lse, ws, ws_bytes, (cudaStream_t)stream, true, true);
+}
+
+int attn_fwd_tiles(const void* q, const void* k, const void* v, const attn_chunk* chunks, int32_t n,
+                   const attn_shape* shape, void* o, float* lse, void* ws, size_t ws_bytes,
+                   void* stream) {
+    return fwd_common(q, k, v, chunks, n, shape, o, lse, ws, ws_bytes, (cudaStream_t)stream, true, false);
+}
+
+int attn_fwd_merge(const attn_chunk* chunks, int32_t n, const attn_shape* shape, void* o, float* lse,
+                   void* ws, size_t ws_bytes, void* stream) {
+    return fwd_common(nullptr, nullptr, nullptr, chunks, n, shape, o, lse, ws, ws_bytes,
+                      (cudaStream_t)stream, false, true);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape, void* dq,
+             void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+    return bwd_common(q, k, v, o, lse, dout, chunks, n, shape, dq, dk, dv, ws, ws_bytes,
+                      (cudaStream_t)stream, kPrep | kTiles | kDq);
+}
+
+int attn_bwd_prep(const void* o, const void* dout, const attn_chunk* chunks, int32_t n,
+                  const attn_shape* shape, void* ws, size_t ws_bytes, void* stream) {
+    return bwd_common(nullptr, nullptr, nullptr, o, nullptr, dout, chunks, n, shape, nullptr, nullptr,
+                      nullptr, ws, ws_bytes, (cudaStream_t)stream, kPrep);
+}
+
+int attn_bwd_tiles(const void* q, const void* k, const void* v, const float* lse, const void* dout,
+                   const attn_chunk* chunks, int32_t n, const attn_shape* shape, void* dk, void* dv,
+                   void* ws, size_t ws_bytes, void* stream) {
+    return bwd_common(q, k, v, nullptr, lse, dout, chunks, n, shape, nullptr, dk, dv, ws, ws_bytes,
+                      (cudaStream_t)stream, kTiles);
+}
+
+int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape, void* dq, void* ws,
+                size_t ws_bytes, void* stream) {
+    return bwd_common(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, chunks, n, shape, dq, nullptr,
+                      nullptr, ws, ws_bytes, (cudaStream_t)stream, kDq);
+}
+
+int attn_status(void* ws, void* stream) {
+    if (!ws) return ATTN_E_INVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_E_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_E_CUDA;
+    if (word) {
+        if (cudaMemsetAsync(ws, 0, sizeof(word), s) != cudaSuccess) return ATTN_E_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_E_CUDA;
+    }
+    return (int)word;
+}
+
+const char* attn_strerror(int st) {
+    switch (st) {
+        case ATTN_OK: return "ok";
+        case ATTN_E_INVAL: return "invalid argument (shape, chunk table, mode or pointer)";
+        case ATTN_E_ALIGN: return "pointer or stride not 16-byte aligned";
+        case ATTN_E_UNSUPPORTED: return "unsupported head dimension or device";
+        case ATTN_E_WORKSPACE: return "workspace missing or too small";
+        case ATTN_E_CUDA: return "CUDA runtime call or kernel launch failed";
+        case ATTN_E_TIMEOUT: return "device wait gave up (bounded wait timed out)";
+        case ATTN_E_BOUNDS: return "device index check failed";
+        case ATTN_E_CAPACITY: return "plan output array too small";
+        default: return "unknown status";
+    }
+}
+
+const char* attn_version(void) { return "libattn 0.1 sm_103a"; }
+
+}  // extern "C"

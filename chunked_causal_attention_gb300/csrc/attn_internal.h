@@ -1,0 +1,109 @@
+// Internal declarations shared by the C-ABI layer and the kernels of libattn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "attn.h"
+
+namespace attn {
+
+constexpr int kTile = 128;            // query rows per forward work item, keys per backward item
+constexpr size_t kHeaderBytes = 256;  // workspace header: status word, counters
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    uint32_t status;      // first device-side error code (ATTN_E_*), 0 if none
+    uint32_t counter[3];  // work counters of persistent kernels
+};
+
+// One forward work item: query rows [r0, r1) against keys [kv_lo, kv_hi)
+// under the causal rule j <= t. part_off < 0: the rows' final O/LSE go to the
+// output tensors; otherwise fp32 O goes to ws_f[part_off + (bh*R + i)*D + d]
+// and LSE to ws_f[part_off + BH*R*D + bh*R + i], i = t - part_row0, R = part_R.
+struct FwdItem {
+    int32_t r0, r1;
+    int32_t kv_lo, kv_hi;
+    int64_t part_off;
+    int32_t part_row0, part_R;
+};
+static_assert(sizeof(FwdItem) == 32, "FwdItem layout");
+
+// Merge segment of one re-split chunk: rows [row0, row0 + R), partial
+// blocks A and B at float offsets off_a, off_b (layout as FwdItem).
+struct MergeSeg {
+    int32_t row0, R;
+    int64_t off_a, off_b;
+    int64_t work0;        // first work index of this segment (rows * BH prefix)
+};
+static_assert(sizeof(MergeSeg) == 32, "MergeSeg layout");
+
+// One backward work item: keys [j0, j1) (j1 - j0 <= 128) of a document
+// that ends at q_end; queries [j0, q_end) see them.
+struct BwdItem {
+    int32_t j0, j1;
+    int32_t q_end;
+    int32_t doc_begin;
+};
+static_assert(sizeof(BwdItem) == 16, "BwdItem layout");
+
+struct Geom {
+    int32_t B, H, T, D;
+    int64_t sb, st, sh;
+    float scale;
+};
+
+struct FwdArgs {
+    const void* q; const void* k; const void* v;
+    void* o; float* lse;
+    float* ws_f;
+    uint32_t* status;
+    const FwdItem* items;
+    int32_t n_items;
+    int32_t group;        // items per head group in the work order
+    Geom g;
+};
+
+struct MergeArgs {
+    void* o; float* lse;
+    const float* ws_f;
+    const MergeSeg* segs;
+    int32_t n_segs;
+    int64_t total_work;   // sum over segments of R * B * H
+    Geom g;
+};
+
+struct PrepArgs {
+    const void* o; const void* dout;
+    float* delta; float* dq_acc;
+    Geom g;
+};
+
+struct BwdArgs {
+    const void* q; const void* k; const void* v; const void* dout;
+    const float* lse; const float* delta;
+    void* dk; void* dv;
+    float* dq_acc;
+    uint32_t* status;
+    const BwdItem* items;
+    int32_t n_items;
+    int32_t group;
+    Geom g;
+};
+
+struct DqArgs {
+    const float* dq_acc;
+    void* dq;
+    Geom g;
+};
+
+// Kernel launchers (return the launch error).
+cudaError_t launch_fwd_tiles(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_tiles(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);
+
+}  // namespace attn

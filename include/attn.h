@@ -1,0 +1,193 @@
+/*
+ * attn.h - C ABI of libattn: chunked causal self-attention on GB300 (sm_103a).
+ *
+ * The operation: causal softmax attention computed subsequence by subsequence.
+ * The query rows of chunk i attend to the resident keys/values of everything
+ * before them (the chunk's context) and to themselves.
+ *   - SPPO, "Efficient Long-sequence LLM Training via Adaptive Sequence Pipeline
+ *     Parallel Offloading": §3.2 (FLOPs-based vs length-based partition), §4
+ *     (multiplexing sequence partition: edge subsequences re-split, results
+ *     combined), §5.1 (attention of subsequence i reads all K/V so far, which
+ *     stay resident on the GPU).
+ *   - InfiniPipe, "Elastic Pipeline Parallelism for Efficient Variable-Length
+ *     Long-Context LLM Training": §II-A (a slice's queries see only preceding
+ *     keys; K/V gradients depend on later slices), §II-B (packed [sum(S), D]
+ *     layout), §III-A1 (chunk = {context C, slice lengths S}).
+ *   - "Sequence Parallelism: Long Sequence Training from System Perspective"
+ *     (blog summary), Deep Dive "Ring Self-Attention": a chunk's output is the
+ *     accumulation of one partial per key/value block.
+ *
+ * Definition computed (one batch row b, head h; scale given by the caller):
+ *   key j is visible to query t  iff  chunk(t).ctx_begin <= j <= t
+ *   LSE_t = ln sum_{j visible} exp(scale * q_t . k_j)
+ *   O_t   = sum_{j visible} exp(scale * q_t . k_j - LSE_t) v_j
+ * and its gradient dQ, dK, dV for an upstream dO.
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers are CUDA device memory owned by the caller. The library
+ *     never allocates, frees or retains device memory; the caller passes a
+ *     workspace sized by attn_workspace_size().
+ *   - q, k, v, o, dout, dq, dk, dv: bf16 (IEEE bfloat16), element (b, t, h, d)
+ *     at  b*sb + t*st + h*sh + d  (strides in elements, d contiguous), the same
+ *     strides for all eight tensors. Dense [B, H, L, D]: sb = H*L*D, sh = L*D,
+ *     st = D. Packed [T, H, D] (B = 1): st = H*D, sh = D.
+ *     Base pointers must be 16-byte aligned and sb, st, sh multiples of 8.
+ *   - lse: fp32, [B][H][T] contiguous, natural log.
+ *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Compute calls only enqueue work and return before it completes.
+ *   - chunks: a HOST array read during the call only.
+ *   - Every call returns an attn status code. Argument errors are detected on
+ *     the host before anything is enqueued. Device-side errors (a bounded wait
+ *     that gave up, an index check that failed) are recorded in the workspace
+ *     and read with attn_status(). No entry point traps or aborts.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ATTN_OK             0
+#define ATTN_E_INVAL        1  /* bad shape, chunk table, mode or pointer      */
+#define ATTN_E_ALIGN        2  /* pointer or stride not 16-byte aligned        */
+#define ATTN_E_UNSUPPORTED  3  /* head dim other than 64 or 128, or no sm_103 */
+#define ATTN_E_WORKSPACE    4  /* workspace NULL or smaller than required      */
+#define ATTN_E_CUDA         5  /* a CUDA runtime call or kernel launch failed  */
+#define ATTN_E_TIMEOUT      6  /* device: a bounded wait gave up               */
+#define ATTN_E_BOUNDS       7  /* device: an index check failed                */
+#define ATTN_E_CAPACITY     8  /* output array of attn_plan* too small          */
+
+/* ---- plan modes (SPPO §3.2, §4) ---------------------------------------- */
+#define ATTN_PLAN_UNIFORM              0  /* length-based: equal 128-multiples  */
+#define ATTN_PLAN_FLOPS                1  /* FLOPs-based: b_k ~ L*sqrt(k/N)     */
+#define ATTN_PLAN_FLOPS_RESPLIT_EDGES  2  /* FLOPS + first/last chunk re-split  */
+
+/* One chunk (InfiniPipe §III-A1 split chunk {C, s}): query rows
+ * [q_begin, q_end) with context C = q_begin - ctx_begin. ctx_begin is the
+ * first visible key (the document start). kv_split = 0: no re-split; else m
+ * with ctx_begin < m < q_end: the chunk's key range is cut into
+ * [ctx_begin, m) and [m, q_end), each computed as a partial and merged by
+ * log-sum-exp (SPPO §4 multiplexing, read as a key/value split). */
+typedef struct {
+    int32_t q_begin, q_end;
+    int32_t ctx_begin;
+    int32_t kv_split;
+} attn_chunk;
+
+typedef struct {
+    int64_t B, H, T, D;   /* batch rows, heads, tokens per row, head dim     */
+    int64_t sb, st, sh;   /* element strides of batch, token, head           */
+    float   scale;        /* softmax scale; usually 1/sqrt(D)                */
+} attn_shape;
+
+/* ---- planning (host only, integer-exact; never touches the GPU) -------- */
+
+/* Chunk boundaries of one causal sequence of L tokens in N chunks.
+ * UNIFORM: b_k = 128*floor(k*L/(128*N)). FLOPS: b_k = the multiple of 128
+ * nearest to L*sqrt(k/N) (ties up), which equalises the quadratic attention
+ * cost of InfiniPipe Eq. (1) (SPPO §3.2 FLOPs-based partition: long chunks
+ * first, short later). b_0 = 0, b_N = L. RESPLIT_EDGES also sets kv_split of
+ * the first and last chunk to q_begin + 128*floor((q_end-q_begin)/256 + 1/2)
+ * when that falls strictly inside the chunk (SPPO §4).
+ * out: host array of cap entries; *n_out = N on success.
+ * Errors: ATTN_E_INVAL (L <= 0, N <= 0, unknown mode, boundaries not strictly
+ * increasing), ATTN_E_CAPACITY (cap < N). */
+int attn_plan(int64_t L, int32_t N, int32_t mode,
+              attn_chunk* out, int32_t cap, int32_t* n_out);
+
+/* Chunks of a packed batch (InfiniPipe §II-B, §III-A1). cu_seqlens: host
+ * array of ndocs+1 non-decreasing offsets, cu_seqlens[0] = 0. A document of
+ * L_d tokens becomes ceil(L_d / max_chunk_tokens) chunks by the mode's rule
+ * measured from the document start, all with ctx_begin = document start;
+ * empty documents give no chunk. RESPLIT_EDGES re-splits the first and last
+ * chunk of the whole plan. Errors as attn_plan. */
+int attn_plan_varlen(const int64_t* cu_seqlens, int32_t ndocs, int32_t max_chunk_tokens,
+                     int32_t mode, attn_chunk* out, int32_t cap, int32_t* n_out);
+
+/* Workspace bytes for pass 0 (forward: attn_fwd and its stages) or pass 1
+ * (backward: attn_bwd and its stages) of this shape and chunk table.
+ * Validates like the compute calls. */
+int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32_t n,
+                        int32_t pass, size_t* bytes);
+
+/* ---- forward ----------------------------------------------------------- */
+
+/* Forward of every chunk: o (bf16) and lse (fp32) for all rows of the
+ * chunks. Chunks must be sorted by q_begin with disjoint query ranges and
+ * 0 <= ctx_begin <= q_begin < q_end <= T. Rows outside every chunk are not
+ * written. Equivalent to attn_fwd_tiles followed by attn_fwd_merge. */
+int attn_fwd(const void* q, const void* k, const void* v,
+             const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+             void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 1 of the forward: the tile kernel. Rows of unsplit chunks (and rows
+ * of split chunks whose tile lies wholly before the split) get their final o
+ * and lse; the two key-range partials of the remaining rows go to the
+ * workspace as fp32. */
+int attn_fwd_tiles(const void* q, const void* k, const void* v,
+                   const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+                   void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 2 of the forward: log-sum-exp merge of the partials of re-split
+ * chunks (RSA accumulation over key/value blocks, made exact with LSE):
+ * LSE = ln(e^{LSE_A} + e^{LSE_B}); O = e^{LSE_A-LSE} O_A + e^{LSE_B-LSE} O_B;
+ * a partial with LSE = -inf has weight 0. A no-op when no chunk is split. */
+int attn_fwd_merge(const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+                   void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- backward ---------------------------------------------------------- */
+
+/* Gradients of the forward for upstream dout, given the forward's o and lse.
+ * The chunk table must partition [0, T) (sorted, contiguous) with every
+ * chunk of one document sharing ctx_begin = the document start; the result
+ * depends on the documents only, not on where chunks are cut (InfiniPipe
+ * §II-A: dK/dV of a token gather contributions of all later tokens).
+ * dq, dk, dv are bf16 with the shared strides. Equivalent to
+ * attn_bwd_prep, attn_bwd_tiles, attn_bwd_dq in that order. */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+             void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 1: D_t = sum_d dO_td * O_td (fp32) into the workspace, and zero the
+ * fp32 dQ accumulator. */
+int attn_bwd_prep(const void* o, const void* dout, const attn_chunk* chunks, int32_t n,
+                  const attn_shape* shape, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 2: one key tile per work item: recompute P = exp(S - LSE), then
+ * dV += P^T dO, dS = P o (dO V^T - D), dK += scale dS^T Q (owned, written as
+ * bf16) and dQ += scale dS K (fp32 reduction into the workspace). */
+int attn_bwd_tiles(const void* q, const void* k, const void* v, const float* lse,
+                   const void* dout, const attn_chunk* chunks, int32_t n,
+                   const attn_shape* shape, void* dk, void* dv,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 3: dq = bf16(fp32 dQ accumulator). */
+int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+                void* dq, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- status ------------------------------------------------------------ */
+
+/* Synchronises `stream`, then reads and clears the device error word in the
+ * workspace header: ATTN_OK, ATTN_E_TIMEOUT or ATTN_E_BOUNDS (or ATTN_E_CUDA
+ * if the read itself fails). The word lives in the first 256 bytes of the
+ * workspace; attn_fwd / attn_fwd_tiles / attn_bwd / attn_bwd_prep clear it
+ * when they start, and a workspace no such call has used must be zeroed by
+ * the caller before its status is read. */
+int attn_status(void* ws, void* stream);
+
+/* Static English text for a status code. */
+const char* attn_strerror(int status);
+
+/* Library version string, e.g. "libattn 0.1 sm_103a". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -129,6 +129,36 @@ def backward(q, k, v, do, scale: float, cu_seqlens=None, row_block: int = 512):
 # Sampled forms for sequences too long for the full oracle.
 # --------------------------------------------------------------------------
 
+def _row_groups(rows, start, max_elems=1 << 27):
+    """Sampled rows sorted and grouped by document, each group small enough
+    that its score matrix (rows x keys) stays under ``max_elems`` entries."""
+    order = np.argsort(rows, kind="stable")
+    groups, cur = [], []
+    for idx in order:
+        t = int(rows[idx])
+        if cur:
+            t0 = int(rows[cur[0]])
+            same_doc = start[t] == start[t0]
+            keys = t - start[t0] + 1
+            if not same_doc or (len(cur) + 1) * keys > max_elems:
+                groups.append(cur)
+                cur = []
+        cur.append(idx)
+    if cur:
+        groups.append(cur)
+    return groups
+
+
+def _rows_probs(q, k, rows_g, s, scale):
+    """Softmax rows P (rows x keys [s, t_max]) of a group of rows of one
+    document; each row is the definition applied to that row alone."""
+    tmax = int(rows_g.max())
+    S = scale * (q[rows_g] @ k[s:tmax + 1].T)
+    j = np.arange(s, tmax + 1)[None, :]
+    S = np.where(j <= rows_g[:, None], S, NEG_INF)
+    return _softmax_rows(S), tmax
+
+
 def forward_rows(q, k, v, rows: Iterable[int], scale: float, cu_seqlens=None):
     """O and LSE of the given query rows only (each row is independent)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -137,14 +167,12 @@ def forward_rows(q, k, v, rows: Iterable[int], scale: float, cu_seqlens=None):
     rows = np.asarray(list(rows), dtype=np.int64)
     O = np.zeros((len(rows), v.shape[1]))
     LSE = np.zeros(len(rows))
-    for i, t in enumerate(rows):
-        s = start[t]
-        S = scale * (k[s:t + 1] @ q[t])
-        mx = S.max()
-        E = np.exp(S - mx)
-        l = E.sum()
-        O[i] = (E / l) @ v[s:t + 1]
-        LSE[i] = mx + np.log(l)
+    for grp in _row_groups(rows, start):
+        rg = rows[grp]
+        s = int(start[rg[0]])
+        (P, lse), tmax = _rows_probs(q, k, rg, s, scale)
+        O[grp] = P @ v[s:tmax + 1]
+        LSE[grp] = lse
     return O, LSE
 
 
@@ -155,17 +183,15 @@ def dq_rows(q, k, v, do, rows: Iterable[int], scale: float, cu_seqlens=None):
     start = doc_start_of_rows(T, cu_seqlens)
     rows = np.asarray(list(rows), dtype=np.int64)
     dq = np.zeros((len(rows), q.shape[1]))
-    for i, t in enumerate(rows):
-        s = start[t]
-        S = scale * (k[s:t + 1] @ q[t])
-        mx = S.max()
-        E = np.exp(S - mx)
-        P = E / E.sum()
-        o = P @ v[s:t + 1]
-        D = do[t] @ o
-        dP = v[s:t + 1] @ do[t]
+    for grp in _row_groups(rows, start):
+        rg = rows[grp]
+        s = int(start[rg[0]])
+        (P, _), tmax = _rows_probs(q, k, rg, s, scale)
+        o = P @ v[s:tmax + 1]
+        D = np.sum(do[rg] * o, axis=1, keepdims=True)
+        dP = do[rg] @ v[s:tmax + 1].T
         dS = P * (dP - D)
-        dq[i] = scale * (dS @ k[s:t + 1])
+        dq[grp] = scale * (dS @ k[s:tmax + 1])
     return dq
 
 

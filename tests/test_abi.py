@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/attn.h declares, its planner equals the oracle's bit for bit, and
+argument errors are reported on the host before anything is enqueued."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+import chunked_causal_attention_gb300 as cca
+from chunked_causal_attention_gb300 import _lib
+from oracle import plan as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "attn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(_lib.LIB_PATH):
+        from chunked_causal_attention_gb300 import build
+        build.build()
+
+
+def test_exports_every_declared_symbol():
+    syms = header_symbols()
+    assert len(syms) >= 13
+    L = cca.lib()
+    for s in syms:
+        assert hasattr(L, s), s
+    assert set(syms) == set(_lib.EXPORTS)
+    assert "sm_103a" in cca.version()
+
+
+def test_plan_matches_oracle_exactly():
+    rng = random.Random(11)
+    cases = [(1024, 4, 0), (32768, 8, 1), (131072, 16, 2), (1 << 20, 64, 1), (1000, 3, 0), (2688, 4, 1)]
+    cases += [(rng.randint(1, 1 << 21), rng.randint(1, 64), rng.randint(0, 2)) for _ in range(400)]
+    for L, N, mode in cases:
+        try:
+            want = P.plan(L, N, mode)
+        except P.PlanError:
+            with pytest.raises(cca.AttnError) as e:
+                cca.attn_plan(L, N, mode)
+            assert e.value.status == 1
+            continue
+        assert cca.attn_plan(L, N, mode) == want, (L, N, mode)
+
+
+def test_plan_varlen_matches_oracle_exactly():
+    rng = random.Random(12)
+    for _ in range(100):
+        nd = rng.randint(1, 12)
+        lens = [rng.choice([0, 1, 5, 127, 128, 129, rng.randint(1, 70000)]) for _ in range(nd)]
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        if cu[-1] == 0:
+            continue
+        mct = rng.choice([128, 1000, 16384])
+        for mode in (0, 1, 2):
+            try:
+                want = P.plan_varlen(cu, mct, mode)
+            except P.PlanError:
+                with pytest.raises(cca.AttnError):
+                    cca.attn_plan_varlen(cu, mct, mode)
+                continue
+            assert cca.attn_plan_varlen(cu, mct, mode) == want
+
+
+def test_plan_errors():
+    L = cca.lib()
+    out = (_lib.attn_chunk * 4)()
+    n = ctypes.c_int32(0)
+    assert L.attn_plan(0, 4, 1, out, 4, ctypes.byref(n)) == 1
+    assert L.attn_plan(1024, 0, 1, out, 4, ctypes.byref(n)) == 1
+    assert L.attn_plan(1024, 4, 7, out, 4, ctypes.byref(n)) == 1
+    assert L.attn_plan(1024, 16, 1, out, 4, ctypes.byref(n)) == 1         # collapsing boundaries
+    assert L.attn_plan(1024, 4, 1, out, 2, ctypes.byref(n)) == 8          # capacity
+    assert L.attn_plan(1024, 4, 1, out, 4, None) == 1
+
+
+def shape(B=1, H=2, T=1024, D=64, scale=0.125):
+    return cca.make_shape(B, H, T, D, H * T * D, D, T * D, scale)
+
+
+def test_workspace_size_validation():
+    ch = cca.attn_plan(1024, 4, 0)
+    assert cca.attn_workspace_size(shape(), ch, 0) >= 256
+    assert cca.attn_workspace_size(shape(), ch, 1) >= 2 * 1024 * 64 * 4
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_workspace_size(shape(D=96), ch, 0)
+    assert e.value.status == 3
+    bad = [(0, 600, 0, 0), (500, 1024, 0, 0)]                  # overlapping
+    with pytest.raises(cca.AttnError):
+        cca.attn_workspace_size(shape(), bad, 0)
+    gap = [(0, 500, 0, 0), (600, 1024, 0, 0)]                  # fine forward, not a partition
+    cca.attn_workspace_size(shape(), gap, 0)
+    with pytest.raises(cca.AttnError):
+        cca.attn_workspace_size(shape(), gap, 1)
+    badsplit = [(0, 1024, 0, 1024)]
+    with pytest.raises(cca.AttnError):
+        cca.attn_workspace_size(shape(), badsplit, 0)
+    baddoc = [(0, 512, 0, 0), (512, 1024, 100, 0)]             # ctx neither continues nor starts a doc
+    with pytest.raises(cca.AttnError):
+        cca.attn_workspace_size(shape(), baddoc, 1)
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_workspace_size(cca.make_shape(1, 2, 1024, 64, 2 * 1024 * 64, 60, 1024 * 64, 0.1), ch, 0)
+    assert e.value.status == 2                                  # token stride not a multiple of 8
+
+
+def test_workspace_partials_sized_for_split_rows():
+    s = cca.make_shape(1, 32, 131072, 128, 32 * 131072 * 128, 128, 131072 * 128, 0.088)
+    ch = cca.attn_plan(131072, 16, 2)
+    unsplit = [(a, b, c, 0) for a, b, c, _ in ch]
+    rows = (32768 - 16384) + (131072 - 129024)
+    extra = cca.attn_workspace_size(s, ch, 0) - cca.attn_workspace_size(s, unsplit, 0)
+    assert extra >= 2 * rows * 32 * (128 + 1) * 4
+
+
+def test_compute_calls_reject_bad_arguments_on_host():
+    """Validation happens before any CUDA call, so these run without a GPU."""
+    L = cca.lib()
+    ch, n = _lib.chunk_array(cca.attn_plan(1024, 4, 0))
+    s = shape()
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    # D unsupported
+    s96 = cca.make_shape(1, 2, 1024, 96, 2 * 1024 * 96, 96, 1024 * 96, 0.1)
+    assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(s96), fake, fake, ws, 1 << 30, None) == 3
+    # misaligned q
+    assert L.attn_fwd(ctypes.c_void_p(4098), fake, fake, ch, n, ctypes.byref(s), fake, fake, ws, 1 << 30, None) == 2
+    # workspace too small / missing
+    assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(s), fake, fake, ws, 16, None) == 4
+    assert L.attn_bwd(fake, fake, fake, fake, fake, fake, ch, n, ctypes.byref(s), fake, fake, fake, None, 0,
+                      None) == 4
+    # null output
+    assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(s), None, fake, ws, 1 << 30, None) == 1
+    # bad chunk table
+    bad, nb = _lib.chunk_array([(0, 2000, 0, 0)])
+    assert L.attn_fwd(fake, fake, fake, bad, nb, ctypes.byref(s), fake, fake, ws, 1 << 30, None) == 1
+    assert L.attn_status(None, None) == 1
+    assert cca.strerror(4).startswith("workspace")

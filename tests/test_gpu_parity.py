@@ -1,0 +1,172 @@
+"""GPU parity, element by element, at sizes the float64 oracle finishes in
+seconds: several 128-row tiles, ragged tails, packed documents down to one
+token, re-split chunks, strided layouts, and the stage entry points.
+Everything runs through the C ABI (libattn.so)."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_attention_gb300 as cca
+from chunked_causal_attention_gb300.workloads import WORKLOADS, make_inputs, workload_inputs
+from oracle import attention as A
+from oracle import plan as P
+
+from parity import check_fwd, check_grad, default_scale, docs_of, head, lse_head, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from chunked_causal_attention_gb300 import build
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    if not os.path.exists(cca._lib.LIB_PATH):
+        build.build()
+
+
+def full_check(q, k, v, do, chunks, packed, scale=None, backward=True, what=""):
+    B = 1 if packed else q.shape[0]
+    H = q.shape[1]
+    D = q.shape[-1]
+    sc = default_scale(D) if scale is None else scale
+    o, lse, dq, dk, dv = run_gpu(q, k, v, do, chunks, packed, scale, backward)
+    cu = docs_of(chunks)
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, doh = (head(x, b, h, packed) for x in (q, k, v, do))
+            if backward:
+                rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, sc, cu)
+            else:
+                ro, rl = A.forward(qh, kh, vh, sc, cu)
+            check_fwd(head(o, b, h, packed), lse_head(lse, b, h), ro, rl, f"{what} b{b}h{h}")
+            if backward:
+                check_grad(head(dq, b, h, packed), rdq, f"{what} dQ b{b}h{h}")
+                check_grad(head(dk, b, h, packed), rdk, f"{what} dK b{b}h{h}")
+                check_grad(head(dv, b, h, packed), rdv, f"{what} dV b{b}h{h}")
+    return o, lse, dq, dk, dv
+
+
+def test_tiny_workload_full():
+    w = WORKLOADS["tiny"]
+    q, k, v, do = (x.cuda() for x in workload_inputs(w))
+    chunks = cca.attn_plan(w.L, w.N, w.mode)
+    assert chunks == P.plan(w.L, w.N, w.mode)
+    full_check(q, k, v, do, chunks, False, what="tiny")
+
+
+@pytest.mark.parametrize("L", [1, 7, 129, 1000])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mode,N", [(0, 1), (0, 3), (1, 2), (2, 1), (2, 3)])
+def test_ragged_dense(L, D, mode, N):
+    try:
+        chunks = P.plan(L, N, mode)
+    except P.PlanError:
+        pytest.skip("plan does not exist for this L")
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 3, L, D, seed=100 + L + D))
+    full_check(q, k, v, do, chunks, False, what=f"L{L} D{D} m{mode} N{N}")
+
+
+def test_token_major_strides():
+    """[B, L, H, D] storage (token stride H*D, head stride D) via the strided ABI."""
+    B, L, H, D = 2, 700, 3, 128
+    base = [x.cuda() for x in make_inputs(B, H, L, D, seed=7)]
+    tm = [x.permute(0, 2, 1, 3).contiguous() for x in base]        # [B, L, H, D]
+    views = [x.permute(0, 2, 1, 3) for x in tm]                      # logical [B, H, L, D] view
+    chunks = P.plan(L, 3, P.FLOPS_RESPLIT_EDGES)
+    o, lse, dq, dk, dv = full_check(*views, chunks, False, what="token-major")
+    o2, lse2, dq2, dk2, dv2 = run_gpu(*base, chunks)
+    assert torch.equal(o.contiguous(), o2) and torch.equal(lse, lse2)
+    assert torch.equal(dk.contiguous(), dk2) and torch.equal(dv.contiguous(), dv2)
+
+
+@pytest.mark.parametrize("mct,mode", [(128, 1), (256, 2), (1000, 0), (16384, 1)])
+def test_packed_documents(mct, mode):
+    lens = [1, 1, 127, 129, 300, 1, 700, 2, 1000]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    try:
+        chunks = P.plan_varlen(cu, mct, mode)
+    except P.PlanError:
+        pytest.skip("no plan")
+    assert cca.attn_plan_varlen(cu, mct, mode) == chunks
+    assert docs_of(chunks) == cu
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 4, cu[-1], 128, seed=21, packed=True))
+    full_check(q, k, v, do, chunks, True, what=f"packed mct{mct} m{mode}")
+
+
+def test_forward_partial_coverage_and_arbitrary_splits():
+    """Chunks that cover part of the rows, with re-split points that are not
+    multiples of 128 and one that lies before q_begin; untouched rows keep
+    their contents."""
+    L, H, D = 1100, 2, 128
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=33))
+    chunks = [(0, 200, 0, 77), (300, 700, 0, 150), (700, 1001, 0, 901), (1001, 1100, 1001, 0)]
+    shape = cca.shape_of(q)
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((1, H, L), 9.0, device=q.device)
+    ws = cca.workspace(shape, chunks, 0)
+    cca.attn_fwd(q, k, v, chunks, shape, o, lse, ws)
+    torch.cuda.synchronize()
+    sc = default_scale(D)
+    for h in range(H):
+        qh, kh, vh = (head(x, 0, h, False) for x in (q, k, v))
+        for qb, qe, cb, m in chunks:
+            ro, rl = A.chunked_forward(qh, kh, vh, [(qb, qe, cb, m)], sc)
+            check_fwd(head(o, 0, h, False)[qb:qe], lse_head(lse, 0, h)[qb:qe], ro[qb:qe], rl[qb:qe], "partial")
+        assert torch.all(o[0, h, 200:300] == 7.0) and torch.all(lse[0, h, 200:300] == 9.0)
+
+
+def test_stage_entry_points_equal_composed_calls():
+    L, H, D = 2000, 2, 128
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=44))
+    chunks = P.plan(L, 3, P.FLOPS_RESPLIT_EDGES)
+    shape = cca.shape_of(q)
+    o, lse = cca.forward(q, k, v, chunks)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    ws = cca.workspace(shape, chunks, 0)
+    cca.attn_fwd_tiles(q, k, v, chunks, shape, o2, lse2, ws)
+    cca.attn_fwd_merge(chunks, shape, o2, lse2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    dq, dk, dv = cca.backward(q, k, v, o, lse, do, chunks)
+    wsb = cca.workspace(shape, chunks, 1)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    cca.attn_bwd_prep(o, do, chunks, shape, wsb)
+    cca.attn_bwd_tiles(q, k, v, lse, do, chunks, shape, dk2, dv2, wsb)
+    cca.attn_bwd_dq(chunks, shape, dq2, wsb)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)       # one CTA owns each key tile
+    assert (dq.float() - dq2.float()).abs().max().item() <= 2e-2   # fp32 atomics: order may differ
+    assert cca.attn_status(ws) == 0 and cca.attn_status(wsb) == 0
+
+
+def test_backward_independent_of_chunk_cuts():
+    L, H, D = 1500, 2, 64
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=55))
+    c1 = P.plan(L, 1, P.FLOPS)
+    c2 = P.plan(L, 5, P.FLOPS_RESPLIT_EDGES)
+    o, lse = cca.forward(q, k, v, c1)
+    _, _, dk1, dv1 = (None,) + cca.backward(q, k, v, o, lse, do, c1)
+    _, _, dk2, dv2 = (None,) + cca.backward(q, k, v, o, lse, do, c2)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+
+
+def test_host_errors_with_device_memory():
+    L, H, D = 512, 1, 128
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=66))
+    chunks = P.plan(L, 2, P.FLOPS)
+    shape = cca.shape_of(q)
+    o, lse = torch.empty_like(q), torch.empty(1, H, L, device="cuda")
+    ws = cca.workspace(shape, chunks, 0)
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_fwd(q, k, v, chunks, shape, o, lse, ws[:16])
+    assert e.value.status == 4
+    flat = torch.empty(q.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    qm = flat[1:].view_as(q)                                   # 2-byte offset: not 16-byte aligned
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_fwd(qm, k, v, chunks, shape, o, lse, ws)
+    assert e.value.status == 2
+    assert cca.attn_status(ws) == 0
