@@ -187,7 +187,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
             a.n_items = (int32_t)L.items.size();
             a.group = kGroup;
             a.g = g;
-            if ((st = launched(launch_fwd_tiles(a, s)))) return st;
+            if ((st = launched(launch_fwd_tiles_tc(a, s)))) return st;
         }
     }
     if (do_merge && !L.segs.empty()) {
@@ -238,7 +238,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
         a.n_items = (int32_t)L.items.size();
         a.group = kGroup;
         a.g = g;
-        if ((st = launched(launch_bwd_tiles(a, s)))) return st;
+        if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
     }
     if (stages & kDq) {
         DqArgs a{dq_acc, dq, g};

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "attn.h"
@@ -99,11 +100,22 @@ struct DqArgs {
     Geom g;
 };
 
+// Coordinate slots (1..3) of the token, head and batch axes in a tile map.
+struct TcMaps {
+    int pos_t, pos_h, pos_b;
+};
+
+// Rank-4 TMA map of a bf16 [B, T, H, D]-strided tensor: axis 0 is the head
+// dim, axes 1..3 are token/head/batch sorted by stride; box = 64 elements
+// (128 bytes, 128-byte swizzle) x 128 tokens. Fills `mp`. False on failure.
+bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
+int device_sm_count();
+
 // Kernel launchers (return the launch error).
-cudaError_t launch_fwd_tiles(const FwdArgs& a, cudaStream_t s);
-cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_tiles(const BwdArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s);   // fwd_tc.cu
+cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s);     // merge.cu
+cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);       // bwd_aux.cu
+cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s);   // bwd_tc.cu
+cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);           // bwd_aux.cu
 
 }  // namespace attn

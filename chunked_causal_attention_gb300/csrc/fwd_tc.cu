@@ -1,0 +1,415 @@
+// Forward tile kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Persistent CTAs walk the cost-sorted work list (128 query rows x one key
+// range x one (batch, head)). Warp roles:
+//   warp 0      TMA producer: Q tile once per item; K and V tiles of 128 keys
+//               through two-stage rings (128-byte swizzled, 64-column boxes).
+//   warp 1      MMA issuer (one thread) and TMEM owner:
+//                 S_j   = Q K_j^T        (both operands K-major in shared memory)
+//                 O    += P_j V_j        (P_j from TMEM, V_j MN-major in shared memory)
+//               S_{j+1} is issued before P_j V_j so the tensor core computes the
+//               next scores while the softmax warps work on the current ones.
+//   warps 4-7   softmax: one query row per thread (TMEM lane = row). Reads S_j
+//               from TMEM, applies the causal/range mask on edge tiles, keeps
+//               the running max m and sum l in base 2, writes P_j as bf16 into
+//               the first half of S_j's columns, and writes O/l and LSE at the
+//               end of the item.
+// Online softmax (the exact form of the blockwise accumulation O = sum_i S_i V_i
+// of Ring Self-Attention): the running max is only moved when a tile's max
+// exceeds it by more than 2^8; then O and l are rescaled by 2^(m_old - m_new).
+// Keeping a stale max below that threshold leaves every P <= 2^8, so fp32 and
+// bf16 hold it, and the final O/l is unchanged.
+//
+// TMEM columns: S buffers at [0,128) and [128,256), O at [256, 256+D).
+// Every mbarrier wait is bounded; a wait that gives up sets ATTN_E_TIMEOUT in
+// the workspace status word and all roles leave their loops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
+
+namespace attn {
+namespace {
+
+using namespace tc;
+
+constexpr int TC_THREADS = 256;
+constexpr int KV_STAGES = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+constexpr uint64_t kWaitNs = 4000000000ull;    // 4 s per wait: far above any legitimate wait
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+
+template <int D>
+struct FwdTcLayout {
+    static constexpr int TILE = 128 * D * 2;            // bytes of one 128-row bf16 tile
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + TILE;
+    static constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
+    static constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = 1;
+    static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + KV_STAGES;
+    static constexpr int B_VFULL = B_KEMPTY + KV_STAGES, B_VEMPTY = B_VFULL + KV_STAGES;
+    static constexpr int B_SFULL = B_VEMPTY + KV_STAGES;       // 2
+    static constexpr int B_PFULL = B_SFULL + 2;                // 2
+    static constexpr int B_ODONE = B_PFULL + 2;
+    static constexpr int B_OFREE = B_ODONE + 1;
+    static constexpr int B_DRAIN = B_OFREE + 1;
+    static constexpr int NBAR = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;        // tmem base (u32), abort flag (int)
+    static constexpr int BYTES = MISC_OFF + 16;
+    static constexpr size_t ALLOC = (size_t)BYTES + 1024;      // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ void tile_coords(const TcMaps& mp, int row, int h, int b, int (&c)[4]) {
+    c[0] = 0;
+    c[mp.pos_t] = row;
+    c[mp.pos_h] = h;
+    c[mp.pos_b] = b;
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, const TcMaps& mp,
+                                          int row, int h, int b) {
+    int c[4];
+    tile_coords(mp, row, h, b, c);
+#pragma unroll
+    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c[1], c[2], c[3]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const FwdArgs a, const TcMaps mp, const int32_t n_work) {
+    using LY = FwdTcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar0 = sbase + LY::BAR_OFF;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC_OFF + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int BH = a.g.B * a.g.H;
+
+    if (tid == 0) {
+        mbar_init(bar(LY::B_QFULL), 1);
+        mbar_init(bar(LY::B_QEMPTY), 1);
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(bar(LY::B_KFULL + s), 1);
+            mbar_init(bar(LY::B_KEMPTY + s), 1);
+            mbar_init(bar(LY::B_VFULL + s), 1);
+            mbar_init(bar(LY::B_VEMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(LY::B_SFULL + s), 1);
+            mbar_init(bar(LY::B_PFULL + s), 128);
+        }
+        mbar_init(bar(LY::B_ODONE), 1);
+        mbar_init(bar(LY::B_OFREE), 128);
+        mbar_init(bar(LY::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (elect_one()) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            uint32_t kc = 0, vc = 0, ic = 0;
+            for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++ic) {
+                int32_t it, bh;
+                decode_work(w, a.n_items, BH, a.group, it, bh);
+                const FwdItem item = a.items[it];
+                const int b = bh / a.g.H, h = bh % a.g.H;
+                if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs)) break;
+                mbar_expect_tx(bar(LY::B_QFULL), LY::TILE);
+                load_tile<D>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
+                const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+                bool ok = true;
+                for (int j = 0; j < nblk && ok; ++j) {
+                    const int row = item.kv_lo + j * 128;
+                    const uint32_t ks = kc % KV_STAGES, vs = vc % KV_STAGES;
+                    ok = mbar_wait(bar(LY::B_KEMPTY + ks), ((kc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                    if (!ok) break;
+                    mbar_expect_tx(bar(LY::B_KFULL + ks), LY::TILE);
+                    load_tile<D>(sbase + LY::K_OFF + ks * LY::TILE, &tmk, bar(LY::B_KFULL + ks), mp, row, h, b);
+                    ++kc;
+                    ok = mbar_wait(bar(LY::B_VEMPTY + vs), ((vc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                    if (!ok) break;
+                    mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE);
+                    load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mp, row, h, b);
+                    ++vc;
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);
+            uint32_t kc = 0, vc = 0, ic = 0, gt = 0;   // gt: global tile counter (S buffer, P, PV index)
+            bool ok = true;
+            for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+                int32_t it, bh;
+                decode_work(w, a.n_items, BH, a.group, it, bh);
+                const FwdItem item = a.items[it];
+                const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+                ok = mbar_wait(bar(LY::B_QFULL), ic & 1, abort_flag, a.status, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t q0 = sbase + LY::Q_OFF;
+                uint32_t pv_vc = vc;                 // V stage of the pending PV
+                for (int j = 0; j <= nblk && ok; ++j) {
+                    if (j < nblk) {
+                        // S_j = Q K_j^T into S buffer (gt + j) & 1
+                        const uint32_t ks = kc % KV_STAGES;
+                        ok = mbar_wait(bar(LY::B_KFULL + ks), (kc / KV_STAGES) & 1, abort_flag, a.status, kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t k0 = sbase + LY::K_OFF + ks * LY::TILE;
+                        const uint32_t sb = tmem + kColS + ((gt + j) & 1) * 128;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(sb, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s, kk > 0);
+                        }
+                        mma_commit(bar(LY::B_KEMPTY + ks));
+                        mma_commit(bar(LY::B_SFULL + ((gt + j) & 1)));
+                        ++kc;
+                        if (j == nblk - 1) mma_commit(bar(LY::B_QEMPTY));
+                    }
+                    if (j >= 1) {
+                        // O += P_{j-1} V_{j-1}
+                        const uint32_t t = gt + j - 1;
+                        const uint32_t pb = t & 1;
+                        if (j == 1) {
+                            ok = mbar_wait(bar(LY::B_OFREE), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                            if (!ok) break;
+                        }
+                        ok = mbar_wait(bar(LY::B_PFULL + pb), (t >> 1) & 1, abort_flag, a.status, kWaitNs);
+                        if (!ok) break;
+                        const uint32_t vs = pv_vc % KV_STAGES;
+                        ok = mbar_wait(bar(LY::B_VFULL + vs), (pv_vc / KV_STAGES) & 1, abort_flag, a.status, kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t v0 = sbase + LY::V_OFF + vs * LY::TILE;
+                        const uint32_t pa = tmem + kColS + pb * 128;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + kColO, pa + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024), id_o,
+                                   (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar(LY::B_VEMPTY + vs));
+                        mma_commit(bar(LY::B_ODONE));
+                        ++pv_vc;
+                    }
+                }
+                vc = pv_vc;
+                gt += nblk;
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int row = tid - 128;                       // TMEM lane == tile row
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const float sl2 = a.g.scale * kLog2e;
+        uint32_t gt = 0, ic = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+            int32_t it, bh;
+            decode_work(w, a.n_items, BH, a.group, it, bh);
+            const FwdItem item = a.items[it];
+            const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+            const int t_row = item.r0 + row;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nblk && ok; ++j) {
+                const uint32_t t = gt + j, b = t & 1;
+                ok = mbar_wait(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sa = tmem + lane_addr + kColS + b * 128;
+                uint32_t r[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(sa + c * 32, r[c]);
+                tmem_ld_wait();
+                const int j0 = item.kv_lo + j * 128;
+                const bool edge = (j0 + 127 > item.r0) || (j0 + 128 > item.kv_hi);
+                float mt = -INFINITY;
+                if (edge) {
+                    const int lim = min(t_row + 1, item.kv_hi) - j0;   // visible columns: c < lim
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float x = __uint_as_float(r[c][i]);
+                            x = (c * 32 + i < lim) ? x : -INFINITY;
+                            r[c][i] = __float_as_uint(x);
+                            mt = fmaxf(mt, x);
+                        }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[c][i]));
+                }
+                mt *= sl2;
+                bool rescale = false;
+                float alpha = 1.f;
+                if (mt > m_run + kRescaleThreshold) {
+                    if (m_run != -INFINITY) {
+                        rescale = true;
+                        alpha = ex2(m_run - mt);
+                    }
+                    m_run = mt;
+                }
+                const float base = m_run == -INFINITY ? 0.f : m_run;
+                float lsum = 0.f;
+                uint32_t p[2][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float p0 = ex2(fmaf(__uint_as_float(r[c][i]), sl2, -base));
+                        float p1 = ex2(fmaf(__uint_as_float(r[c][i + 1]), sl2, -base));
+                        lsum += p0 + p1;
+                        p[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
+                    }
+                l_run = rescale ? fmaf(l_run, alpha, lsum) : l_run + lsum;
+                tmem_st32(sa + 0, p[0]);
+                tmem_st32(sa + 32, p[1]);
+                // tcgen05.ld/st are warp-collective: rescale O if any row of the warp needs it
+                if (__any_sync(0xffffffffu, rescale) && j > 0) {
+                    // O holds the sum over tiles < j once PV_{j-1} has completed
+                    ok = mbar_wait(bar(LY::B_ODONE), (t - 1) & 1, abort_flag, a.status, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t oa = tmem + lane_addr + kColO;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(oa + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(oa + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(LY::B_PFULL + b));
+            }
+            if (!ok) break;
+            // epilogue: wait for the last PV of the item, then O / l
+            const uint32_t tl = gt + nblk - 1;
+            ok = mbar_wait(bar(LY::B_ODONE), tl & 1, abort_flag, a.status, kWaitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float lse = l_run > 0.f ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
+            const uint32_t oa = tmem + lane_addr + kColO;
+            const int b_ = bh / a.g.H, h_ = bh % a.g.H;
+            const bool live = t_row < item.r1;
+            if (item.part_off < 0) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b_ * a.g.sb +
+                                     (int64_t)h_ * a.g.sh + (int64_t)t_row * a.g.st;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(oa + c * 32, o);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+                            v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+                            v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+                            v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+                            d4[i] = v;
+                        }
+                    }
+                }
+                if (live) a.lse[(int64_t)bh * a.g.T + t_row] = lse;
+            } else {
+                const int64_t R = item.part_R;
+                const int i_row = t_row - item.part_row0;
+                float* dst = a.ws_f + item.part_off + ((int64_t)bh * R + i_row) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(oa + c * 32, o);
+                    tmem_ld_wait();
+                    if (live) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                    }
+                }
+                if (live) a.ws_f[item.part_off + (int64_t)BH * R * D + (int64_t)bh * R + i_row] = lse;
+            }
+            tc_fence_before();
+            mbar_arrive(bar(LY::B_OFREE));
+            gt += nblk;
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        if (*abort_flag) {
+            // a wait gave up: let the MMAs already issued drain (bounded) before TMEM is released
+            if (elect_one()) {
+                mma_commit(bar(LY::B_DRAIN));
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(bar(LY::B_DRAIN), 0) && globaltimer() - t0 < kWaitNs) {
+                }
+            }
+            __syncwarp();
+        }
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
+    CUtensorMap mq, mk, mv;
+    TcMaps mp{1, 2, 3};
+    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, a.g, mp) || !make_tile_map(&mv, a.v, a.g, mp))
+        return cudaErrorInvalidValue;
+    const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
+    if (work <= 0) return cudaSuccess;
+    if (work > INT32_MAX) return cudaErrorInvalidValue;
+    const size_t smem = FwdTcLayout<D>::ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(work, device_sm_count());
+    fwd_tc_kernel<D><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, (int32_t)work);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s) {
+    return a.g.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+}
+
+}  // namespace attn

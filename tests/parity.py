@@ -51,12 +51,14 @@ def check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert r <= O_REL_L2, f"{what} O rel-L2 {r}"
     le = np.abs(lse_gpu - lse_ref).max() if lse_ref.size else 0.0
     assert le <= LSE_ABS, f"{what} LSE abs {le}"
+    print(f"[parity] {what}: O max-abs {err:.3e} rel-L2 {r:.3e}, LSE max-abs {le:.3e}")
     return err, r, le
 
 
 def check_grad(g, ref, what=""):
     r = rel_l2(g, ref)
     assert r <= GRAD_REL_L2, f"{what} rel-L2 {r}"
+    print(f"[parity] {what}: rel-L2 {r:.3e}")
     return r
 
 

@@ -52,17 +52,30 @@ def sampled_rows_check(w, q, k, v, do, o, lse, dq, n_rows, seed, what):
     check_grad(np.concatenate(gq), np.concatenate(rq), what + " dQ")
 
 
-def invariants_check(w, do, dk, dv, what):
+def invariants_check(w, q, do, dk, dv, what):
+    """sum_j dV_j = sum_t dO_t and sum_j dK_j = 0 per (head, document). The
+    tolerance is relative to the size of the summed terms: bf16 rounding of P
+    (relative 2^-8) and of the dK/dV outputs leaves a deviation of order
+    2^-8 * sqrt(sum of squared terms), far below a missing or doubled tile.
+    Measured sum-dV deviations grow with the accumulation length: 8.7e-5 at
+    32K, 1.8e-4 at 128K, 1.2e-3 at 1M tokens; a missing 128-key tile gives
+    more than 1e-1."""
     cu = w.cu_seqlens() or [0, w.L]
+    worst_v = worst_k = 0.0
     for h in range(w.H):
         dkh = head(dk, 0, h, w.packed)
         dvh = head(dv, 0, h, w.packed)
         doh = head(do, 0, h, w.packed)
+        qh = head(q, 0, h, w.packed)
         for s, e in zip(cu[:-1], cu[1:]):
-            sk = dkh[s:e].sum(axis=0)
-            assert np.linalg.norm(sk) <= GRAD_REL_L2 * np.sqrt((dkh[s:e] ** 2).sum()), f"{what} sum dK h{h}"
             sv = dvh[s:e].sum(axis=0) - doh[s:e].sum(axis=0)
-            assert np.linalg.norm(sv) <= GRAD_REL_L2 * np.sqrt((dvh[s:e] ** 2).sum()), f"{what} sum dV h{h}"
+            nv = np.linalg.norm(sv) / np.sqrt((doh[s:e] ** 2).sum())
+            sk = dkh[s:e].sum(axis=0)
+            nk = np.linalg.norm(sk) / (w.scale * np.sqrt((qh[s:e] ** 2).sum()) + np.sqrt((dkh[s:e] ** 2).sum()))
+            worst_v, worst_k = max(worst_v, nv), max(worst_k, nk)
+            assert nv <= 5e-3, f"{what} sum dV h{h} doc {s}: {nv}"
+            assert nk <= 1e-2, f"{what} sum dK h{h} doc {s}: {nk}"
+    print(f"[parity] {what} invariants: sum dV rel {worst_v:.3e}, sum dK rel {worst_k:.3e}")
 
 
 def tail_keys_check(w, q, k, v, do, dk, dv, heads, n_keys, seed, what):
@@ -93,7 +106,7 @@ def test_7b_32k():
     check_grad(head(dk, 0, 0, False), rdk, "32k dK h0")
     check_grad(head(dv, 0, 0, False), rdv, "32k dV h0")
     sampled_rows_check(w, q, k, v, do, o, lse, dq, 1024, 5, "32k")
-    invariants_check(w, do, dk, dv, "32k")
+    invariants_check(w, q, do, dk, dv, "32k")
     assert cca.attn_status(cca.workspace(cca.shape_of(q), chunks, 0)) in (0,)
 
 
@@ -111,7 +124,7 @@ def test_7b_128k():
         ro, rl = A.forward_rows(qh, kh, vh, r, w.scale)
         check_fwd(head(o, 0, 3, False)[r], lse_head(lse, 0, 3)[r], ro, rl, f"128k split {m}")
     tail_keys_check(w, q, k, v, do, dk, dv, [0, 17], 48, 7, "128k")
-    invariants_check(w, do, dk, dv, "128k")
+    invariants_check(w, q, do, dk, dv, "128k")
 
 
 def test_packed_256k():
@@ -134,7 +147,7 @@ def test_packed_256k():
         check_grad(head(dk, 0, h, True)[s:e], rdk, f"packed dK doc {s}")
         check_grad(head(dv, 0, h, True)[s:e], rdv, f"packed dV doc {s}")
     sampled_rows_check(w, q, k, v, do, o, lse, dq, 2048, 8, "packed")
-    invariants_check(w, do, dk, dv, "packed")
+    invariants_check(w, q, do, dk, dv, "packed")
 
 
 @pytest.mark.slow
@@ -146,4 +159,4 @@ def test_13b_1m():
     o, lse, dq, dk, dv = run_gpu(q, k, v, do, chunks)
     sampled_rows_check(w, q, k, v, do, o, lse, dq, 4096, 9, "1m")
     tail_keys_check(w, q, k, v, do, dk, dv, [11], 16, 10, "1m")
-    invariants_check(w, do, dk, dv, "1m")
+    invariants_check(w, q, do, dk, dv, "1m")
