@@ -158,7 +158,11 @@ int check_ws(void* ws, size_t have, size_t need) {
     return ATTN_OK;
 }
 
-constexpr int32_t kGroup = 8;
+// Items per head group in the work order (see decode_work): the forward's
+// items of one head read the same K/V tiles, so bigger groups raise L2 reuse;
+// the backward's items share Q/dO tiles and dQ rows.
+constexpr int32_t kGroupFwd = 32;
+constexpr int32_t kGroupBwd = 8;
 
 int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* chunks, int32_t n,
                const attn_shape* shape, void* o, float* lse, void* ws, size_t ws_bytes,
@@ -185,7 +189,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
             a.status = (uint32_t*)ws;
             a.items = (const FwdItem*)(w + L.off_items);
             a.n_items = (int32_t)L.items.size();
-            a.group = kGroup;
+            a.group = kGroupFwd;
             a.g = g;
             if ((st = launched(launch_fwd_tiles_tc(a, s)))) return st;
         }
@@ -236,7 +240,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
         a.dk = dk; a.dv = dv; a.dq_acc = dq_acc; a.status = (uint32_t*)ws;
         a.items = (const BwdItem*)(w + L.off_items);
         a.n_items = (int32_t)L.items.size();
-        a.group = kGroup;
+        a.group = kGroupBwd;
         a.g = g;
         if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
     }

@@ -2,7 +2,9 @@
 //
 // One work item = 128 keys [j0, j1) of one (batch, head); the item walks the
 // query blocks of 128 rows that can see those keys (queries t >= j0 up to the
-// document end): a key's dK/dV collect the contributions of every later
+// document end) from the last block down to the diagonal one, so the CTAs
+// working on one head meet the same Q/dO tiles and dQ rows at about the same
+// time and both stay in L2: a key's dK/dV collect the contributions of every later
 // token of its sequence (InfiniPipe §II-A: K/V gradients of a token depend on
 // all subsequent tokens). Persistent CTAs take items from the cost-sorted list.
 //
@@ -52,9 +54,10 @@ struct BwdTcLayout {
     static constexpr int BAR_OFF = DLT_OFF + 512;
     static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
     static constexpr int B_QFULL = 2, B_QEMPTY = 4;       // 2 each
-    static constexpr int B_SDP = 6, B_PFULL = 7, B_DQFULL = 8, B_DQFREE = 9;
-    static constexpr int B_DKDVFULL = 10, B_DKDVFREE = 11, B_DRAIN = 12;
-    static constexpr int NBAR = 13;
+    static constexpr int B_SDP = 6, B_PCH = 7;            // B_PCH + c: P^T/dS^T of query chunk c ready
+    static constexpr int B_DQFULL = 11, B_DQFREE = 12;
+    static constexpr int B_DKDVFULL = 13, B_DKDVFREE = 14, B_DRAIN = 15;
+    static constexpr int NBAR = 16;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr size_t ALLOC = (size_t)BYTES + 1024;
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             mbar_init(bar(LY::B_QEMPTY + s), 1);
         }
         mbar_init(bar(LY::B_SDP), 1);
-        mbar_init(bar(LY::B_PFULL), 128);
+        for (int c = 0; c < 4; ++c) mbar_init(bar(LY::B_PCH + c), 128);
         mbar_init(bar(LY::B_DQFULL), 1);
         mbar_init(bar(LY::B_DQFREE), 128);
         mbar_init(bar(LY::B_DKDVFULL), 1);
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, kWaitNs);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_QFULL + s), 2 * LY::TILE);
-                    const int row = item.j0 + i * 128;
+                    const int row = item.j0 + (nq - 1 - i) * 128;
                     load_tile_b<D>(sbase + LY::Q_OFF + s * LY::TILE, &tmq, bar(LY::B_QFULL + s), mp, row, h, b);
                     load_tile_b<D>(sbase + LY::DO_OFF + s * LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, h, b);
                 }
@@ -195,22 +198,25 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                                kk > 0);
                     }
                     mma_commit(bar(LY::B_SDP));
-                    ok = mbar_wait(bar(LY::B_PFULL), gb & 1, abort_flag, a.status, kWaitNs);
-                    if (!ok) break;
-                    tc_fence_after();
                     if (i == 0) {
                         ok = mbar_wait(bar(LY::B_DKDVFREE), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
                         if (!ok) break;
-                        tc_fence_after();
                     }
+                    // dV += P^T dO and dK += dS^T Q, 32 queries (two k-steps) at a time as the
+                    // softmax-gradient warps finish each chunk
+                    for (int c = 0; c < 4 && ok; ++c) {
+                        ok = mbar_wait(bar(LY::B_PCH + c), gb & 1, abort_flag, a.status, kWaitNs);
+                        if (!ok) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(o0 + kk * 2048, 16384, 1024), id_g,
-                               (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_sw128(q0 + kk * 2048, 16384, 1024), id_g,
-                               (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 2 * c; kk < 2 * c + 2; ++kk) {
+                            mma_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(o0 + kk * 2048, 16384, 1024), id_g,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                            mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_sw128(q0 + kk * 2048, 16384, 1024),
+                                   id_g, (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    if (!ok) break;
                     mma_commit(bar(LY::B_QEMPTY + s));
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const float* L = Lg + (int64_t)bh * a.g.T;
             const float* Dl = a.delta + (int64_t)bh * a.g.T;
             for (int i = 0; i < nq; ++i, ++gb) {
-                const int i0 = item.j0 + i * 128;
+                const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
                 named_sync(1, 128);
                 {
                     const int q = i0 + krow;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     if (!ok) break;
                 }
                 tc_fence_after();
-                const bool edge = (i == 0) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
+                const bool edge = (i0 == item.j0) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t sr[32], dr[32];
@@ -293,11 +299,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                         uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
                         *reinterpret_cast<uint4*>(atom + ((chunk ^ (krow & 7)) << 4)) = v;
                     }
+                    tmem_st_wait();
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(bar(LY::B_PCH + c));
                 }
-                tmem_st_wait();
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(bar(LY::B_PFULL));
             }
             if (!ok) break;
             // epilogue: dK * scale, dV as bf16
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 tc_fence_after();
-                const int q = item.j0 + i * 128 + qrow;
+                const int q = item.j0 + (nq - 1 - i) * 128 + qrow;
                 const bool live = q < item.q_end;
                 float* dst = dQg + (int64_t)q * D;
 #pragma unroll

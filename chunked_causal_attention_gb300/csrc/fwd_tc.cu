@@ -56,7 +56,8 @@ struct FwdTcLayout {
     static constexpr int B_PFULL = B_SFULL + 2;                // 2
     static constexpr int B_ODONE = B_PFULL + 2;
     static constexpr int B_OFREE = B_ODONE + 1;
-    static constexpr int B_DRAIN = B_OFREE + 1;
+    static constexpr int B_OFULL = B_OFREE + 1;                // last PV of an item complete
+    static constexpr int B_DRAIN = B_OFULL + 1;
     static constexpr int NBAR = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;        // tmem base (u32), abort flag (int)
     static constexpr int BYTES = MISC_OFF + 16;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         mbar_init(bar(LY::B_ODONE), 1);
         mbar_init(bar(LY::B_OFREE), 128);
+        mbar_init(bar(LY::B_OFULL), 1);
         mbar_init(bar(LY::B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                    (j - 1 > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(bar(LY::B_VEMPTY + vs));
                         mma_commit(bar(LY::B_ODONE));
+                        if (j == nblk) mma_commit(bar(LY::B_OFULL));
                         ++pv_vc;
                     }
                 }
@@ -313,9 +316,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mbar_arrive(bar(LY::B_PFULL + b));
             }
             if (!ok) break;
-            // epilogue: wait for the last PV of the item, then O / l
-            const uint32_t tl = gt + nblk - 1;
-            ok = mbar_wait(bar(LY::B_ODONE), tl & 1, abort_flag, a.status, kWaitNs);
+            // epilogue: wait for the last PV of the item, then O / l. This uses the
+            // once-per-item barrier: when the softmax warps get here up to two PVs
+            // may still be in flight, more than a per-PV parity wait can tell apart.
+            ok = mbar_wait(bar(LY::B_OFULL), ic & 1, abort_flag, a.status, kWaitNs);
             if (!ok) break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

@@ -305,3 +305,50 @@ def causal_flops(pairs: int, D: int) -> Tuple[int, int]:
     """Algorithmic FLOPs of (forward, backward) for ``pairs`` visible (t, j)
     pairs: 2 GEMMs forward (QK^T, PV) and 5 backward (S, dP, dV, dK, dQ)."""
     return 4 * D * pairs, 10 * D * pairs
+
+
+# --------------------------------------------------------------------------
+# Closed form for periodic keys: a full-size check of every row and key.
+# --------------------------------------------------------------------------
+
+def periodic_keys(q, kc, v, do, scale: float):
+    """O, LSE, dQ and dV of one causal sequence whose keys repeat with period
+    p: k_j = kc[j mod p]. Then the scores of row t take only p values
+    s_tc = scale q_t . kc[c], so with n_c(t) = #{j <= t : j mod p = c}:
+
+        Z_t = sum_c n_c(t) e^{s_tc},   LSE_t = ln Z_t,   W_tc = e^{s_tc} / Z_t = P_tj (j in class c)
+        O_t  = sum_c W_tc CV_c(t),     CV_c(t) = sum_{j <= t, j = c mod p} v_j
+        dQ_t = scale sum_c W_tc (dO_t . CV_c(t) - n_c(t) D_t) kc[c],   D_t = dO_t . O_t
+        dV_j = sum_{t >= j} W_{t, j mod p} dO_t
+
+    i.e. the definition regrouped by key class, evaluated with cumulative
+    sums in O(T p D). dK is not produced (it needs D x D running sums)."""
+    q, kc, v, do = _f64(q), _f64(kc), _f64(v), _f64(do)
+    T, D = q.shape
+    p = kc.shape[0]
+    t = np.arange(T)
+    n = np.stack([np.where(t >= c, (t - c) // p + 1, 0) for c in range(p)], axis=1).astype(np.float64)
+    s = scale * (q @ kc.T)
+    s = np.where(n > 0, s, NEG_INF)
+    M = s.max(axis=1)
+    E = np.where(n > 0, np.exp(s - M[:, None]), 0.0)
+    Z = (n * E).sum(axis=1)
+    LSE = M + np.log(Z)
+    W = E / Z[:, None]
+    O = np.zeros((T, D))
+    g = np.zeros((T, p))
+    cls = t % p
+    CVs = []
+    for c in range(p):
+        CV = np.cumsum(np.where((cls == c)[:, None], v, 0.0), axis=0)
+        O += W[:, c:c + 1] * CV
+        CVs.append(CV)
+    Dt = np.sum(do * O, axis=1)
+    for c in range(p):
+        g[:, c] = np.sum(do * CVs[c], axis=1) - n[:, c] * Dt
+    dQ = scale * ((W * g) @ kc)
+    dV = np.zeros((T, D))
+    for c in range(p):
+        R = np.cumsum((W[:, c:c + 1] * do)[::-1], axis=0)[::-1]
+        dV[cls == c] = R[cls == c]
+    return O, LSE, dQ, dV

@@ -160,3 +160,29 @@ def test_13b_1m():
     sampled_rows_check(w, q, k, v, do, o, lse, dq, 4096, 9, "1m")
     tail_keys_check(w, q, k, v, do, dk, dv, [11], 16, 10, "1m")
     invariants_check(w, q, do, dk, dv, "1m")
+
+
+@pytest.mark.parametrize("name", ["7b_128k", pytest.param("13b_1m", marks=pytest.mark.slow)])
+def test_periodic_keys_every_row_and_key(name):
+    """Keys repeating with period 3 (k_j = kc[j mod 3]) make the float64 oracle
+    linear in T (oracle.attention.periodic_keys), so O, LSE, dQ are checked on
+    every row and dV on every key at full size, including the first keys whose
+    dV sums over the whole sequence."""
+    from chunked_causal_attention_gb300.workloads import randn_bf16
+    w = WORKLOADS[name]
+    q, _, v, do = workload_inputs(w, device="cuda")
+    p = 3
+    kc = randn_bf16((w.B, w.H, p, w.D), w.seed * 4 + 7, device="cuda")
+    k = kc[:, :, torch.arange(w.L, device="cuda") % p, :].contiguous()
+    chunks = plan_of(w)
+    o, lse, dq, dk, dv = run_gpu(q, k, v, do, chunks)
+    for h in (0, w.H - 1):
+        kch = kc[0, h].float().cpu().numpy().astype(np.float64)
+        ro, rl, rdq, rdv = A.periodic_keys(head(q, 0, h, False), kch, head(v, 0, h, False), head(do, 0, h, False),
+                                           w.scale)
+        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"{name} periodic h{h} all rows")
+        gdq, gdv = head(dq, 0, h, False), head(dv, 0, h, False)
+        check_grad(gdq, rdq, f"{name} periodic dQ h{h} all rows")
+        check_grad(gdv, rdv, f"{name} periodic dV h{h} all keys")
+        check_grad(gdv[:4096], rdv[:4096], f"{name} periodic dV h{h} first 4096 keys")
+        check_grad(gdv[-4096:], rdv[-4096:], f"{name} periodic dV h{h} last 4096 keys")

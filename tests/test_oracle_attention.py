@@ -235,3 +235,15 @@ def test_flop_count():
     assert pairs == 131072 * 131073 // 2 == 8590000128
     f, b = A.causal_flops(pairs * 32, 128)
     assert f + b == 14 * 128 * 32 * pairs
+
+
+@pytest.mark.parametrize("T,p,D", [(700, 3, 16), (257, 1, 8), (130, 7, 32)])
+def test_periodic_keys_closed_form_matches_definition(T, p, D):
+    q, v, do = rand((T, D), 81), rand((T, D), 82), rand((T, D), 83)
+    kc = rand((p, D), 84)
+    k = kc[np.arange(T) % p]
+    sc = 1 / math.sqrt(D)
+    dq, dk, dv, O, L = A.backward(q, k, v, do, sc, None, row_block=64)
+    Op, Lp, dqp, dvp = A.periodic_keys(q, kc, v, do, sc)
+    for a, b in ((Op, O), (Lp, L), (dqp, dq), (dvp, dv)):
+        np.testing.assert_allclose(a, b, atol=1e-10, rtol=1e-10)
