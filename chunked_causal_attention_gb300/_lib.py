@@ -26,7 +26,10 @@ PLAN_FLOPS_RESPLIT_EDGES = 2
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
-           "attn_status", "attn_strerror", "attn_version")
+           "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
+
+# Size of the library-held scratch area of attn_fwd_noalloc (ATTN_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class AttnError(RuntimeError):
@@ -66,6 +69,7 @@ _SIG = {
     "attn_bwd_tiles": ([_VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
                        ctypes.c_int),
     "attn_bwd_dq": ([_CP, _I32, _SP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_fwd_noalloc": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP], ctypes.c_int),
     "attn_status": ([_VP, _VP], ctypes.c_int),
     "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "attn_version": ([], ctypes.c_char_p),
@@ -212,6 +216,14 @@ def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
     arr, n = chunk_array(chunks)
     _check("attn_bwd_dq", lib().attn_bwd_dq(arr, n, ctypes.byref(shape), _ptr(dq), _ptr(ws),
                                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_fwd_noalloc(q, k, v, chunks, shape, o, lse, stream=None) -> None:
+    """Forward without a workspace argument: for callers that cannot allocate
+    device memory; uses the library's own scratch (see include/attn.h)."""
+    arr, n = chunk_array(chunks)
+    _check("attn_fwd_noalloc", lib().attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape),
+                                                      _ptr(o), _ptr(lse), _stream(stream)))
 
 
 def attn_status(ws, stream=None) -> int:

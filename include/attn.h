@@ -170,6 +170,34 @@ int attn_bwd_tiles(const void* q, const void* k, const void* v, const float* lse
 int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                 void* dq, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- forward without a caller-provided workspace ----------------------- */
+
+/* Bytes of the scratch area inside the library used by attn_fwd_noalloc. */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* The forward (as attn_fwd) for callers that cannot allocate device memory,
+ * e.g. code hosted by a runtime that owns all device memory and offers no
+ * allocator, or code that must not allocate once it is running. The pages
+ * have no counterpart: this is a convenience of this library.
+ * Instead of a workspace argument it uses a scratch area of
+ * ATTN_NOALLOC_SCRATCH_BYTES that lives in the library and that every GPU
+ * which loads the library holds until the process exits. The caller still
+ * passes q, k, v, o and lse; arguments, layouts and errors are as attn_fwd.
+ * Returns ATTN_E_WORKSPACE when this shape and chunk table need more forward
+ * workspace than ATTN_NOALLOC_SCRATCH_BYTES (attn_workspace_size, pass 0);
+ * re-split chunks need fp32 partials, so they reach the limit first.
+ * The first call on a device looks up the scratch address for that device
+ * (with that device current); make that first call before any stream
+ * capture. It allocates nothing. All calls share the one scratch area and
+ * it keeps the last call's contents (every call rewrites what it reads):
+ * calls that overlap on the GPU race with each other, so issue them on one
+ * stream, or otherwise one after the other. The device status word of this
+ * path (ATTN_E_TIMEOUT / ATTN_E_BOUNDS) lives in that library scratch, which
+ * attn_status() cannot be pointed at, so it is not readable by the caller. */
+int attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                     const attn_chunk* chunks, int32_t n, const attn_shape* shape,
+                     void* o, float* lse, void* stream);
+
 /* ---- status ------------------------------------------------------------ */
 
 /* Synchronises `stream`, then reads and clears the device error word in the
