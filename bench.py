@@ -33,6 +33,33 @@ METRIC = "causal attn fwd+bwd TFLOP/s (bf16) at L=128K, % of GB300 dense BF16 pe
 CPU_SAMPLE_TOKENS = 40960     # causal prefix of one head timed on the host cores
 
 
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic_7b_128k.json")
+KERNEL_SOURCES = ["bwd_tc.cu", "attn_api.cpp", "device_common.cuh", "tc_common.cuh", "attn_internal.h"]
+
+
+def kernel_source_hash():
+    """SHA-256 over the sources that define the backward tile kernel and its work order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "chunked_causal_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch of the backward tile kernel from the committed ncu
+    capture, or None when the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("workload") != workload or t.get("source_sha256") != kernel_source_hash():
+        return None
+    return t["dram_bytes_read"] + t["dram_bytes_write"]
+
+
 def load_peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -314,7 +341,8 @@ def run_ours(args):
             "roofline": {"kernel": "bwd key-tile kernel (attn_bwd_tiles)", "bound": "tensor",
                          "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
                          "peak_kind": f"bf16_tflops_sustained ({peak_src})",
-                         "frac_of_burst": achieved / peak_burst, "traffic": None},
+                         "frac_of_burst": achieved / peak_burst, "traffic": measured_traffic(w.name),
+                         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
             "gpu_launches": launches_per_step * args.steps,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},

@@ -158,11 +158,13 @@ int check_ws(void* ws, size_t have, size_t need) {
     return ATTN_OK;
 }
 
-// Items per head group in the work order (see decode_work): the forward's
-// items of one head read the same K/V tiles, so bigger groups raise L2 reuse;
-// the backward's items share Q/dO tiles and dQ rows.
+// Items per head group in the work order (see decode_work). The forward's
+// items of one head read the same K/V tiles, so bigger groups raise L2 reuse.
+// The backward runs head-major (one group = all items of a head): every dQ
+// row of a head receives one fp32 reduction per key tile, and with all CTAs
+// on the same head those reductions and the shared Q/dO tiles stay in L2.
 constexpr int32_t kGroupFwd = 32;
-constexpr int32_t kGroupBwd = 8;
+constexpr int32_t kGroupBwd = 1 << 30;
 
 int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* chunks, int32_t n,
                const attn_shape* shape, void* o, float* lse, void* ws, size_t ws_bytes,

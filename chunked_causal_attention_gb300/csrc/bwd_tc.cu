@@ -246,15 +246,27 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const int key = item.j0 + krow;
             const float* L = Lg + (int64_t)bh * a.g.T;
             const float* Dl = a.delta + (int64_t)bh * a.g.T;
+            // LSE and D_t of the next query block are fetched one block ahead into
+            // registers, so the global-load latency stays off the critical path
+            float next_l = 0.f, next_d = 0.f;
+            {
+                const int q = item.j0 + (nq - 1) * 128 + krow;
+                if (q < item.q_end) {
+                    next_l = L[q] * kLog2e;
+                    next_d = Dl[q];
+                }
+            }
             for (int i = 0; i < nq; ++i, ++gb) {
                 const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
                 named_sync(1, 128);
-                {
-                    const int q = i0 + krow;
-                    s_lse[krow] = q < item.q_end ? L[q] * kLog2e : 0.f;
-                    s_dlt[krow] = q < item.q_end ? Dl[q] : 0.f;
-                }
+                s_lse[krow] = next_l;
+                s_dlt[krow] = next_d;
                 named_sync(1, 128);
+                if (i + 1 < nq) {
+                    const int q = i0 - 128 + krow;             // next block (always inside the document)
+                    next_l = L[q] * kLog2e;
+                    next_d = Dl[q];
+                }
                 ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 if (gb > 0) {
@@ -359,24 +371,27 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 const int q = item.j0 + (nq - 1 - i) * 128 + qrow;
                 const bool live = q < item.q_end;
                 float* dst = dQg + (int64_t)q * D;
+                // copy the dQ row out of TMEM, release the columns at once, then
+                // send the reductions: the next block's dP^T can start while the
+                // fp32 adds drain through L2
+                uint32_t r[D / 32][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + kColDP + c * 32, r);
-                    tmem_ld_wait();
-                    if (live) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            float4 v = make_float4(__uint_as_float(r[4 * u]) * a.g.scale,
-                                                   __uint_as_float(r[4 * u + 1]) * a.g.scale,
-                                                   __uint_as_float(r[4 * u + 2]) * a.g.scale,
-                                                   __uint_as_float(r[4 * u + 3]) * a.g.scale);
-                            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * u), v);
-                        }
-                    }
-                }
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_addr + kColDP + c * 32, r[c]);
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(bar(LY::B_DQFREE));
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            float4 v = make_float4(__uint_as_float(r[c][4 * u]) * a.g.scale,
+                                                   __uint_as_float(r[c][4 * u + 1]) * a.g.scale,
+                                                   __uint_as_float(r[c][4 * u + 2]) * a.g.scale,
+                                                   __uint_as_float(r[c][4 * u + 3]) * a.g.scale);
+                            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * u), v);
+                        }
+                }
             }
         }
     }
