@@ -109,6 +109,9 @@ struct TcMaps {
 // dim, axes 1..3 are token/head/batch sorted by stride; box = 64 elements
 // (128 bytes, 128-byte swizzle) x 128 tokens. Fills `mp`. False on failure.
 bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
+// Rank-3 TMA map of the fp32 dQ accumulator [B*H][T][D]: box of 32 floats
+// (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g);
 int device_sm_count();
 
 // Kernel launchers (return the launch error).

@@ -2,30 +2,36 @@
 //
 // One work item = 128 keys [j0, j1) of one (batch, head); the item walks the
 // query blocks of 128 rows that can see those keys (queries t >= j0 up to the
-// document end) from the last block down to the diagonal one, so the CTAs
-// working on one head meet the same Q/dO tiles and dQ rows at about the same
-// time and both stay in L2: a key's dK/dV collect the contributions of every later
-// token of its sequence (InfiniPipe §II-A: K/V gradients of a token depend on
-// all subsequent tokens). Persistent CTAs take items from the cost-sorted list.
+// document end) from the last block down to the diagonal one: a key's dK/dV
+// collect the contributions of every later token of its sequence (InfiniPipe
+// §II-A: K/V gradients of a token depend on all subsequent tokens). Persistent
+// CTAs take items head-major (all CTAs on one head at a time), so the head's
+// Q/dO tiles and dQ accumulator rows are reused from L2.
 //
-// Warp roles:
-//   warp 0      TMA producer: K, V once per item; Q and dO per query block
-//               through a two-stage ring.
-//   warp 1      MMA issuer (one thread) and TMEM owner. Per query block:
-//                 S^T  = K Q^T     -> TMEM [0,128)      (SS, both K-major)
-//                 dP^T = V dO^T    -> TMEM [128,256)    (SS, both K-major)
-//                 dV  += P^T dO    -> TMEM dV           (A = P^T in TMEM, B = dO MN-major)
-//                 dK  += dS^T Q    -> TMEM dK           (A = dS^T in TMEM, B = Q MN-major)
-//                 dQ   = dS K      -> TMEM [128,128+D)  (A = dS MN-major in shared memory,
-//                                                        B = K MN-major)
-//   warps 4-7   softmax gradient, one key row per thread (TMEM lane = key):
-//                 P^T  = 2^(S^T * scale*log2 e - LSE_t*log2 e)   (zero where t < key or t >= end)
-//                 dS^T = P^T o (dP^T - D_t)
-//               P^T and dS^T go back to TMEM as bf16 (A operands of dV, dK), dS
-//               also to shared memory for dQ; at the end of the item these
-//               warps write dK * scale and dV as bf16.
-//   warps 8-11  dQ drain, one query row per thread: dQ * scale from TMEM,
-//               added into the fp32 workspace accumulator with vector atomics.
+// Warp roles (16 warps):
+//   warp 0       TMA producer: K, V once per item; Q and dO of a query block into
+//                one 2-tile stage of a two-stage ring.
+//   warp 1       MMA issuer (one thread) and TMEM owner. Per query block:
+//                  S^T  = K Q^T     -> TMEM [0,128)      (SS, both K-major)
+//                  dP^T = V dO^T    -> TMEM [128,256)    (SS, both K-major)
+//                  dV  += P^T dO    -> TMEM [256,256+D)  (A = P^T in TMEM, B = dO MN-major)
+//                  dK  += dS^T Q    -> TMEM dK           (A = dS^T in TMEM, B = Q MN-major)
+//                  dQ   = dS K      -> TMEM [128,128+D)  (A = dS MN-major in shared memory,
+//                                                         B = K MN-major)
+//   warps 4-7    softmax gradient for query columns [0,64), one key row per thread
+//   warps 8-11   softmax gradient for query columns [64,128):
+//                  P^T  = 2^(S^T * scale*log2 e - LSE_t*log2 e)   (zero where t < key or t >= end)
+//                  dS^T = P^T o (dP^T - D_t)
+//                P^T and dS^T of a 32-column chunk go back into that chunk's own
+//                TMEM columns as bf16 (A operands of dV, dK); dS also goes to
+//                shared memory for dQ. The MMA thread consumes chunks as they
+//                are released. At the end of the item warps 4-7 write dK*scale
+//                and warps 8-11 write dV.
+//   warps 12-15  dQ drain, one query row per thread: dQ*scale from TMEM into the
+//                block's Q/dO stage (free once the block's MMAs are done; the
+//                fp32 tile is exactly its size), then one thread issues TMA
+//                reduce-adds into the fp32 accumulator and hands the stage back
+//                to the producer once the TMA engine has read it.
 // Every mbarrier wait is bounded (ATTN_E_TIMEOUT in the status word).
 #include "tc_common.cuh"
 
@@ -34,7 +40,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int BT_THREADS = 384;
+constexpr int BT_THREADS = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColDP = 128;
@@ -43,18 +49,18 @@ constexpr uint64_t kWaitNs = 4000000000ull;
 
 template <int D>
 struct BwdTcLayout {
-    static constexpr int TILE = 128 * D * 2;
+    static constexpr int TILE = 128 * D * 2;           // one 128-row bf16 tile
+    static constexpr int STAGE = 2 * TILE;             // Q + dO of a block; also the fp32 dQ staging
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + TILE;
-    static constexpr int Q_OFF = V_OFF + TILE;            // 2 stages
-    static constexpr int DO_OFF = Q_OFF + 2 * TILE;       // 2 stages
-    static constexpr int DS_OFF = DO_OFF + 2 * TILE;      // 128 keys x 128 queries bf16, MN-major
-    static constexpr int LSE_OFF = DS_OFF + 32768;        // 128 floats (LSE * log2 e)
-    static constexpr int DLT_OFF = LSE_OFF + 512;         // 128 floats (D_t)
-    static constexpr int BAR_OFF = DLT_OFF + 512;
+    static constexpr int QDO_OFF = V_OFF + TILE;       // 2 stages
+    static constexpr int DS_OFF = QDO_OFF + 2 * STAGE; // 128 keys x 128 queries bf16, MN-major
+    static constexpr int NL_OFF = DS_OFF + 32768;      // 128 floats: -LSE_t * log2 e
+    static constexpr int ND_OFF = NL_OFF + 512;        // 128 floats: -D_t
+    static constexpr int BAR_OFF = ND_OFF + 512;
     static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
-    static constexpr int B_QFULL = 2, B_QEMPTY = 4;       // 2 each
-    static constexpr int B_SDP = 6, B_PCH = 7;            // B_PCH + c: P^T/dS^T of query chunk c ready
+    static constexpr int B_QFULL = 2, B_QEMPTY = 4;    // 2 each
+    static constexpr int B_SDP = 6, B_PCH = 7;         // B_PCH + c: P^T/dS^T of query chunk c ready
     static constexpr int B_DQFULL = 11, B_DQFREE = 12;
     static constexpr int B_DKDVFULL = 13, B_DKDVFREE = 14, B_DRAIN = 15;
     static constexpr int NBAR = 16;
@@ -82,8 +88,8 @@ __device__ __forceinline__ void load_tile_b(uint32_t dst, const CUtensorMap* map
 template <int D>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a,
-                  const TcMaps mp, const int32_t n_work) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                  const __grid_constant__ CUtensorMap tmdq, const BwdArgs a, const TcMaps mp, const int32_t n_work) {
     using LY = BwdTcLayout<D>;
     constexpr uint32_t kColDK = kColDV + D;
     extern __shared__ uint8_t smem_raw[];
@@ -93,8 +99,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC_OFF + 4);
-    float* s_lse = reinterpret_cast<float*>(sm + LY::LSE_OFF);
-    float* s_dlt = reinterpret_cast<float*>(sm + LY::DLT_OFF);
+    float* s_nl = reinterpret_cast<float*>(sm + LY::NL_OFF);
+    float* s_nd = reinterpret_cast<float*>(sm + LY::ND_OFF);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int BH = a.g.B * a.g.H;
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         mbar_init(bar(LY::B_DQFULL), 1);
         mbar_init(bar(LY::B_DQFREE), 128);
         mbar_init(bar(LY::B_DKDVFULL), 1);
-        mbar_init(bar(LY::B_DKDVFREE), 128);
+        mbar_init(bar(LY::B_DKDVFREE), 256);
         mbar_init(bar(LY::B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -149,10 +155,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     const uint32_t s = qc & 1;
                     ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, kWaitNs);
                     if (!ok) break;
-                    mbar_expect_tx(bar(LY::B_QFULL + s), 2 * LY::TILE);
+                    mbar_expect_tx(bar(LY::B_QFULL + s), LY::STAGE);
                     const int row = item.j0 + (nq - 1 - i) * 128;
-                    load_tile_b<D>(sbase + LY::Q_OFF + s * LY::TILE, &tmq, bar(LY::B_QFULL + s), mp, row, h, b);
-                    load_tile_b<D>(sbase + LY::DO_OFF + s * LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, h, b);
+                    const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
+                    load_tile_b<D>(st, &tmq, bar(LY::B_QFULL + s), mp, row, h, b);
+                    load_tile_b<D>(st + LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, h, b);
                 }
             }
         }
@@ -178,8 +185,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     ok = mbar_wait(bar(LY::B_QFULL + s), (qc >> 1) & 1, abort_flag, a.status, kWaitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t q0 = sbase + LY::Q_OFF + s * LY::TILE;
-                    const uint32_t o0 = sbase + LY::DO_OFF + s * LY::TILE;
+                    const uint32_t q0 = sbase + LY::QDO_OFF + s * LY::STAGE;
+                    const uint32_t o0 = q0 + LY::TILE;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -202,22 +209,24 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                         ok = mbar_wait(bar(LY::B_DKDVFREE), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
                         if (!ok) break;
                     }
-                    // dV += P^T dO and dK += dS^T Q, 32 queries (two k-steps) at a time as the
-                    // softmax-gradient warps finish each chunk
-                    for (int c = 0; c < 4 && ok; ++c) {
+                    // dV += P^T dO and dK += dS^T Q one 32-query chunk (two k-steps) at a
+                    // time, in the order the two softmax-gradient groups release them
+                    for (int n = 0; n < 4 && ok; ++n) {
+                        const int c = (n & 1) * 2 + (n >> 1);     // 0, 2, 1, 3
                         ok = mbar_wait(bar(LY::B_PCH + c), gb & 1, abort_flag, a.status, kWaitNs);
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
-                        for (int kk = 2 * c; kk < 2 * c + 2; ++kk) {
-                            mma_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(o0 + kk * 2048, 16384, 1024), id_g,
-                                   (i > 0 || kk > 0) ? 1u : 0u);
-                            mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, sdesc_sw128(q0 + kk * 2048, 16384, 1024),
-                                   id_g, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int h = 0; h < 2; ++h) {
+                            const int kk = 2 * c + h;
+                            const uint32_t acc = (i > 0 || n > 0 || h > 0) ? 1u : 0u;
+                            mma_ts(tmem + kColDV, tmem + kColS + 32 * c + 8 * h,
+                                   sdesc_sw128(o0 + kk * 2048, 16384, 1024), id_g, acc);
+                            mma_ts(tmem + kColDK, tmem + kColDP + 32 * c + 8 * h,
+                                   sdesc_sw128(q0 + kk * 2048, 16384, 1024), id_g, acc);
                         }
                     }
                     if (!ok) break;
-                    mma_commit(bar(LY::B_QEMPTY + s));
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ss(tmem + kColDP, sdesc_sw128(ds0 + kk * 2048, 16384, 1024),
@@ -229,44 +238,39 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 mma_commit(bar(LY::B_DKDVFULL));
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax gradient + dK/dV epilogue
-        const int krow = tid - 128;
+        const int grp = (warp - 4) >> 2;                 // 0: query columns [0,64), 1: [64,128)
+        const int krow = tid - 128 - 128 * grp;          // TMEM lane == key row
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const float sl2 = a.g.scale * kLog2e;
-        const float* Lg = a.lse + 0;
+        const float2 sl2x2 = make_float2(sl2, sl2);
         uint32_t gb = 0, ic = 0;
         bool ok = true;
-        uint8_t* ds_row = sm + LY::DS_OFF + krow * 128;
+        uint8_t* ds_row = sm + LY::DS_OFF + grp * 16384 + krow * 128;
+        // this thread stages one value per block: -LSE*log2e (krow < 64) or -D_t of
+        // query 64*grp + (krow & 63), fetched one block ahead
+        const bool stage_l = krow < 64;
+        float* stage_dst = (stage_l ? s_nl : s_nd) + 64 * grp + (krow & 63);
         for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
             int32_t it, bh;
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const BwdItem item = a.items[it];
             const int nq = (item.q_end - item.j0 + 127) / 128;
             const int key = item.j0 + krow;
-            const float* L = Lg + (int64_t)bh * a.g.T;
-            const float* Dl = a.delta + (int64_t)bh * a.g.T;
-            // LSE and D_t of the next query block are fetched one block ahead into
-            // registers, so the global-load latency stays off the critical path
-            float next_l = 0.f, next_d = 0.f;
+            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.g.T;
+            const float mul = stage_l ? -kLog2e : -1.f;
+            float next = 0.f;
             {
-                const int q = item.j0 + (nq - 1) * 128 + krow;
-                if (q < item.q_end) {
-                    next_l = L[q] * kLog2e;
-                    next_d = Dl[q];
-                }
+                const int q = item.j0 + (nq - 1) * 128 + 64 * grp + (krow & 63);
+                if (q < item.q_end) next = src[q] * mul;
             }
             for (int i = 0; i < nq; ++i, ++gb) {
                 const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
-                named_sync(1, 128);
-                s_lse[krow] = next_l;
-                s_dlt[krow] = next_d;
-                named_sync(1, 128);
-                if (i + 1 < nq) {
-                    const int q = i0 - 128 + krow;             // next block (always inside the document)
-                    next_l = L[q] * kLog2e;
-                    next_d = Dl[q];
-                }
+                named_sync(1 + grp, 128);
+                *stage_dst = next;
+                named_sync(1 + grp, 128);
+                if (i + 1 < nq) next = src[i0 - 128 + 64 * grp + (krow & 63)] * mul;
                 ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 if (gb > 0) {
@@ -277,39 +281,48 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 tc_fence_after();
                 const bool edge = (i0 == item.j0) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int h = 0; h < 2; ++h) {
+                    const int c = 2 * grp + h;
                     uint32_t sr[32], dr[32];
                     tmem_ld32(tmem + lane_addr + kColS + c * 32, sr);
                     tmem_ld32(tmem + lane_addr + kColDP + c * 32, dr);
                     tmem_ld_wait();
+                    const float4* nl4 = reinterpret_cast<const float4*>(s_nl + c * 32);
+                    const float4* nd4 = reinterpret_cast<const float4*>(s_nd + c * 32);
                     uint32_t pp[16], dd[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pv[2], dv[2];
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 L4 = nl4[e4], D4 = nd4[e4];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int ql = c * 32 + e + u;
-                            float p = ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse[ql]));
+                            const int e = 4 * e4 + 2 * u;
+                            const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
+                            const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
+                            const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                   sl2x2, nl);
+                            float p0 = ex2(x.x), p1 = ex2(x.y);
                             if (edge) {
-                                const int q = i0 + ql;
-                                const bool vis = key <= q && q < item.q_end && key < item.j1;
-                                p = vis ? p : 0.f;
+                                const int q = i0 + c * 32 + e;
+                                const bool key_ok = key < item.j1;
+                                p0 = (key_ok && key <= q && q < item.q_end) ? p0 : 0.f;
+                                p1 = (key_ok && key <= q + 1 && q + 1 < item.q_end) ? p1 : 0.f;
                             }
-                            pv[u] = p;
-                            dv[u] = p * (__uint_as_float(dr[e + u]) - s_dlt[ql]);
+                            const float2 dpv = fadd2(
+                                make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd);
+                            const float2 ds = fmul2(make_float2(p0, p1), dpv);
+                            pp[e >> 1] = pack_bf16(p0, p1);
+                            dd[e >> 1] = pack_bf16(ds.x, ds.y);
                         }
-                        pp[e >> 1] = pack_bf16(pv[0], pv[1]);
-                        dd[e >> 1] = pack_bf16(dv[0], dv[1]);
                     }
-                    tmem_st16(tmem + lane_addr + kColS + c * 16, pp);
-                    tmem_st16(tmem + lane_addr + kColDP + c * 16, dd);
+                    // P^T and dS^T into the first 16 columns of this chunk's own S^T / dP^T columns
+                    tmem_st16(tmem + lane_addr + kColS + c * 32, pp);
+                    tmem_st16(tmem + lane_addr + kColDP + c * 32, dd);
                     // dS row (this key) for queries [32c, 32c+32): 4 chunks of 16 bytes, 128-byte swizzle
-                    uint8_t* atom = ds_row + (c >> 1) * 16384;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int chunk = (c & 1) * 4 + u;
+                        const int chunk = h * 4 + u;
                         uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                        *reinterpret_cast<uint4*>(atom + ((chunk ^ (krow & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (krow & 7)) << 4)) = v;
                     }
                     tmem_st_wait();
                     fence_proxy_async_smem();
@@ -318,44 +331,42 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 }
             }
             if (!ok) break;
-            // epilogue: dK * scale, dV as bf16
+            // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16)
             ok = mbar_wait(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, kWaitNs);
             if (!ok) break;
             tc_fence_after();
             const int b_ = bh / a.g.H, h_ = bh % a.g.H;
             const int64_t roff = (int64_t)b_ * a.g.sb + (int64_t)h_ * a.g.sh + (int64_t)key * a.g.st;
             const bool live = key < item.j1;
+            const uint32_t col = grp == 0 ? kColDK : kColDV;
+            const float gmul = grp == 0 ? a.g.scale : 1.f;
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(grp == 0 ? a.dk : a.dv) + roff;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? kColDK : kColDV;
-                const float mul = which == 0 ? a.g.scale : 1.f;
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? a.dk : a.dv) + roff;
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + col + c * 32, r);
+                tmem_ld_wait();
+                if (live) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + col + c * 32, r);
-                    tmem_ld_wait();
-                    if (live) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(r[8 * u + 0]) * mul, __uint_as_float(r[8 * u + 1]) * mul);
-                            v.y = pack_bf16(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul);
-                            v.z = pack_bf16(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul);
-                            v.w = pack_bf16(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul);
-                            d4[u] = v;
-                        }
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(r[8 * u + 0]) * gmul, __uint_as_float(r[8 * u + 1]) * gmul);
+                        v.y = pack_bf16(__uint_as_float(r[8 * u + 2]) * gmul, __uint_as_float(r[8 * u + 3]) * gmul);
+                        v.z = pack_bf16(__uint_as_float(r[8 * u + 4]) * gmul, __uint_as_float(r[8 * u + 5]) * gmul);
+                        v.w = pack_bf16(__uint_as_float(r[8 * u + 6]) * gmul, __uint_as_float(r[8 * u + 7]) * gmul);
+                        d4[u] = v;
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(bar(LY::B_DKDVFREE));
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain
-        const int qrow = tid - 256;
+        const int qrow = tid - 384;
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const float sc = a.g.scale;
         uint32_t gb = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x) {
@@ -363,37 +374,49 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const BwdItem item = a.items[it];
             const int nq = (item.q_end - item.j0 + 127) / 128;
-            float* dQg = a.dq_acc + (int64_t)bh * a.g.T * D;
             for (int i = 0; i < nq; ++i, ++gb) {
+                const int i0 = item.j0 + (nq - 1 - i) * 128;
+                const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
+                uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 tc_fence_after();
-                const int q = item.j0 + (nq - 1 - i) * 128 + qrow;
-                const bool live = q < item.q_end;
-                float* dst = dQg + (int64_t)q * D;
-                // copy the dQ row out of TMEM, release the columns at once, then
-                // send the reductions: the next block's dP^T can start while the
-                // fp32 adds drain through L2
-                uint32_t r[D / 32][32];
+                // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32 columns)
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_addr + kColDP + c * 32, r[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(bar(LY::B_DQFREE));
-                if (live) {
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    uint32_t r[2][32];
+                    tmem_ld32(tmem + lane_addr + kColDP + (2 * hh) * 32, r[0]);
+                    tmem_ld32(tmem + lane_addr + kColDP + (2 * hh + 1) * 32, r[1]);
+                    tmem_ld_wait();
+                    if (hh == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(LY::B_DQFREE));      // TMEM columns free for the next dP^T
+                    }
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c)
+                    for (int x = 0; x < 2; ++x) {
+                        uint8_t* sub = stage + (2 * hh + x) * 16384 + qrow * 128;
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            float4 v = make_float4(__uint_as_float(r[c][4 * u]) * a.g.scale,
-                                                   __uint_as_float(r[c][4 * u + 1]) * a.g.scale,
-                                                   __uint_as_float(r[c][4 * u + 2]) * a.g.scale,
-                                                   __uint_as_float(r[c][4 * u + 3]) * a.g.scale);
-                            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * u), v);
+                            float4 v = make_float4(__uint_as_float(r[x][4 * u]) * sc, __uint_as_float(r[x][4 * u + 1]) * sc,
+                                                   __uint_as_float(r[x][4 * u + 2]) * sc,
+                                                   __uint_as_float(r[x][4 * u + 3]) * sc);
+                            *reinterpret_cast<float4*>(sub + ((u ^ (qrow & 7)) << 4)) = v;
                         }
+                    }
+                }
+                fence_proxy_async_smem();
+                named_sync(3, 128);
+                if (qrow == 0) {
+                    const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0, bh);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                    mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage
                 }
             }
         }
+        if (qrow == 0) bulk_wait_all();
     }
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
@@ -416,10 +439,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 
 template <int D>
 cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     TcMaps mp{1, 2, 3};
     if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, a.g, mp) || !make_tile_map(&mv, a.v, a.g, mp) ||
-        !make_tile_map(&mdo, a.dout, a.g, mp))
+        !make_tile_map(&mdo, a.dout, a.g, mp) || !make_dq_acc_map(&mdq, a.dq_acc, a.g))
         return cudaErrorInvalidValue;
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
     if (work <= 0) return cudaSuccess;
@@ -428,7 +451,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_tc_kernel<D><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, a, mp, (int32_t)work);
+    bwd_tc_kernel<D><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, (int32_t)work);
     return cudaGetLastError();
 }
 
