@@ -260,17 +260,19 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const int key = item.j0 + krow;
             const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.g.T;
             const float mul = stage_l ? -kLog2e : -1.f;
+            // raw value of the next block, scaled only when it is staged, so the
+            // load's latency is not waited for until then
             float next = 0.f;
             {
                 const int q = item.j0 + (nq - 1) * 128 + 64 * grp + (krow & 63);
-                if (q < item.q_end) next = src[q] * mul;
+                if (q < item.q_end) next = src[q];
             }
             for (int i = 0; i < nq; ++i, ++gb) {
                 const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
                 named_sync(1 + grp, 128);
-                *stage_dst = next;
+                *stage_dst = next * mul;
                 named_sync(1 + grp, 128);
-                if (i + 1 < nq) next = src[i0 - 128 + 64 * grp + (krow & 63)] * mul;
+                if (i + 1 < nq) next = src[i0 - 128 + 64 * grp + (krow & 63)];
                 ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 if (gb > 0) {
@@ -283,46 +285,54 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int c = 2 * grp + h;
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_addr + kColS + c * 32, sr);
-                    tmem_ld32(tmem + lane_addr + kColDP + c * 32, dr);
-                    tmem_ld_wait();
-                    const float4* nl4 = reinterpret_cast<const float4*>(s_nl + c * 32);
-                    const float4* nd4 = reinterpret_cast<const float4*>(s_nd + c * 32);
-                    uint32_t pp[16], dd[16];
+                    // the chunk's 32 queries in two halves of 16 columns (keeps the live
+                    // registers low enough for the compiler to interleave the pairs)
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 L4 = nl4[e4], D4 = nd4[e4];
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int col = c * 32 + hf * 16;
+                        uint32_t sr[16], dr[16];
+                        tmem_ld16(tmem + lane_addr + kColS + col, sr);
+                        tmem_ld16(tmem + lane_addr + kColDP + col, dr);
+                        tmem_ld_wait();
+                        const float4* nl4 = reinterpret_cast<const float4*>(s_nl + col);
+                        const float4* nd4 = reinterpret_cast<const float4*>(s_nd + col);
+                        uint32_t pp[8], dd[8];
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const float4 L4 = nl4[e4], D4 = nd4[e4];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int e = 4 * e4 + 2 * u;
+                                const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
+                                const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
+                                const float2 x = ffma2(
+                                    make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nl);
+                                float p0 = ex2(x.x), p1 = ex2(x.y);
+                                if (edge) {
+                                    const int q = i0 + col + e;
+                                    const bool key_ok = key < item.j1;
+                                    p0 = (key_ok && key <= q && q < item.q_end) ? p0 : 0.f;
+                                    p1 = (key_ok && key <= q + 1 && q + 1 < item.q_end) ? p1 : 0.f;
+                                }
+                                const float2 dpv = fadd2(
+                                    make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd);
+                                const float2 ds = fmul2(make_float2(p0, p1), dpv);
+                                pp[e >> 1] = pack_bf16(p0, p1);
+                                dd[e >> 1] = pack_bf16(ds.x, ds.y);
+                            }
+                        }
+                        // P^T and dS^T (8 columns per half) into the first 16 columns of
+                        // this chunk's own S^T / dP^T columns
+                        tmem_st8(tmem + lane_addr + kColS + c * 32 + hf * 8, pp);
+                        tmem_st8(tmem + lane_addr + kColDP + c * 32 + hf * 8, dd);
+                        // dS row (this key) for these 16 queries: 2 chunks of 16 bytes,
+                        // 128-byte swizzle
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int e = 4 * e4 + 2 * u;
-                            const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
-                            const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
-                            const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                                   sl2x2, nl);
-                            float p0 = ex2(x.x), p1 = ex2(x.y);
-                            if (edge) {
-                                const int q = i0 + c * 32 + e;
-                                const bool key_ok = key < item.j1;
-                                p0 = (key_ok && key <= q && q < item.q_end) ? p0 : 0.f;
-                                p1 = (key_ok && key <= q + 1 && q + 1 < item.q_end) ? p1 : 0.f;
-                            }
-                            const float2 dpv = fadd2(
-                                make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd);
-                            const float2 ds = fmul2(make_float2(p0, p1), dpv);
-                            pp[e >> 1] = pack_bf16(p0, p1);
-                            dd[e >> 1] = pack_bf16(ds.x, ds.y);
+                            const int chunk = h * 4 + hf * 2 + u;
+                            uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+                            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (krow & 7)) << 4)) = v;
                         }
-                    }
-                    // P^T and dS^T into the first 16 columns of this chunk's own S^T / dP^T columns
-                    tmem_st16(tmem + lane_addr + kColS + c * 32, pp);
-                    tmem_st16(tmem + lane_addr + kColDP + c * 32, dd);
-                    // dS row (this key) for queries [32c, 32c+32): 4 chunks of 16 bytes, 128-byte swizzle
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int chunk = h * 4 + u;
-                        uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (krow & 7)) << 4)) = v;
                     }
                     tmem_st_wait();
                     fence_proxy_async_smem();
@@ -381,27 +391,24 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, kWaitNs);
                 if (!ok) break;
                 tc_fence_after();
-                // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32 columns)
+                // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32
+                // columns), one sub-tile at a time; the TMEM columns are released after
+                // the last load
 #pragma unroll
-                for (int hh = 0; hh < D / 64; ++hh) {
-                    uint32_t r[2][32];
-                    tmem_ld32(tmem + lane_addr + kColDP + (2 * hh) * 32, r[0]);
-                    tmem_ld32(tmem + lane_addr + kColDP + (2 * hh + 1) * 32, r[1]);
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + kColDP + cc * 32, r);
                     tmem_ld_wait();
-                    if (hh == D / 64 - 1) {
+                    if (cc == D / 32 - 1) {
                         tc_fence_before();
                         mbar_arrive(bar(LY::B_DQFREE));      // TMEM columns free for the next dP^T
                     }
+                    uint8_t* sub = stage + cc * 16384 + qrow * 128;
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        uint8_t* sub = stage + (2 * hh + x) * 16384 + qrow * 128;
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            float4 v = make_float4(__uint_as_float(r[x][4 * u]) * sc, __uint_as_float(r[x][4 * u + 1]) * sc,
-                                                   __uint_as_float(r[x][4 * u + 2]) * sc,
-                                                   __uint_as_float(r[x][4 * u + 3]) * sc);
-                            *reinterpret_cast<float4*>(sub + ((u ^ (qrow & 7)) << 4)) = v;
-                        }
+                    for (int u = 0; u < 8; ++u) {
+                        float4 v = make_float4(__uint_as_float(r[4 * u]) * sc, __uint_as_float(r[4 * u + 1]) * sc,
+                                               __uint_as_float(r[4 * u + 2]) * sc, __uint_as_float(r[4 * u + 3]) * sc);
+                        *reinterpret_cast<float4*>(sub + ((u ^ (qrow & 7)) << 4)) = v;
                     }
                 }
                 fence_proxy_async_smem();

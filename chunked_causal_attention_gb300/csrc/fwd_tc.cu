@@ -264,10 +264,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             mt = fmaxf(mt, x);
                         }
                 } else {
+                    // four independent chains of three-input maxima
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[c][i]));
+                        for (int i = 0; i < 32; i += 2)
+                            m4[c] = fmax3(m4[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+                    mt = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
                 }
                 mt *= sl2;
                 bool rescale = false;
@@ -280,17 +284,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     m_run = mt;
                 }
                 const float base = m_run == -INFINITY ? 0.f : m_run;
-                float lsum = 0.f;
+                // exponents two at a time (f32x2 FMA), row sum in two paired accumulators
+                const float2 sl2x2 = make_float2(sl2, sl2), nbase = make_float2(-base, -base);
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 uint32_t p[2][32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        float p0 = ex2(fmaf(__uint_as_float(r[c][i]), sl2, -base));
-                        float p1 = ex2(fmaf(__uint_as_float(r[c][i + 1]), sl2, -base));
-                        lsum += p0 + p1;
+                        const float2 x =
+                            ffma2(make_float2(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), sl2x2, nbase);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        acc[(i >> 1) & 1] = fadd2(acc[(i >> 1) & 1], make_float2(p0, p1));
                         p[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
                     }
+                const float lsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
                 l_run = rescale ? fmaf(l_run, alpha, lsum) : l_run + lsum;
                 tmem_st32(sa + 0, p[0]);
                 tmem_st32(sa + 32, p[1]);
