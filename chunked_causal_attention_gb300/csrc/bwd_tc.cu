@@ -85,6 +85,75 @@ __device__ __forceinline__ void load_tile_b(uint32_t dst, const CUtensorMap* map
     for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c[1], c[2], c[3]);
 }
 
+// Softmax gradient of one query block for one warpgroup (query columns
+// [64*grp, 64*grp+64)) as four half-chunks of 16 columns; the TMEM loads of the
+// next half-chunk are in flight while the current one is computed. EDGE adds
+// the causal/document/ragged-tile mask (diagonal block, partial last block,
+// last key tile of a document); interior blocks skip it.
+template <bool EDGE>
+__device__ __forceinline__ void sg_block(uint32_t tm, int grp, int krow, int key, int i0, const BwdItem& item,
+                                         const float* s_nl, const float* s_nd, uint8_t* ds_row, float2 sl2x2,
+                                         uint32_t bar_pch) {
+    uint32_t sr[2][16], dr[2][16];
+    tmem_ld16(tm + kColS + grp * 64, sr[0]);
+    tmem_ld16(tm + kColDP + grp * 64, dr[0]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int h = k >> 1, hf = k & 1;
+        const int c = 2 * grp + h;
+        const int col = c * 32 + hf * 16;
+        const int b = k & 1;
+        tmem_ld_wait();
+        if (k + 1 < 4) {
+            const int ncol = (2 * grp + ((k + 1) >> 1)) * 32 + ((k + 1) & 1) * 16;
+            tmem_ld16(tm + kColS + ncol, sr[b ^ 1]);
+            tmem_ld16(tm + kColDP + ncol, dr[b ^ 1]);
+        }
+        const float4* nl4 = reinterpret_cast<const float4*>(s_nl + col);
+        const float4* nd4 = reinterpret_cast<const float4*>(s_nd + col);
+        uint32_t pp[8], dd[8];
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 L4 = nl4[e4], D4 = nd4[e4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = 4 * e4 + 2 * u;
+                const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
+                const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
+                const float2 x = ffma2(make_float2(__uint_as_float(sr[b][e]), __uint_as_float(sr[b][e + 1])), sl2x2, nl);
+                float p0 = ex2(x.x), p1 = ex2(x.y);
+                if (EDGE) {
+                    const int q = i0 + col + e;
+                    const bool key_ok = key < item.j1;
+                    p0 = (key_ok && key <= q && q < item.q_end) ? p0 : 0.f;
+                    p1 = (key_ok && key <= q + 1 && q + 1 < item.q_end) ? p1 : 0.f;
+                }
+                const float2 dpv = fadd2(make_float2(__uint_as_float(dr[b][e]), __uint_as_float(dr[b][e + 1])), nd);
+                const float2 ds = fmul2(make_float2(p0, p1), dpv);
+                pp[e >> 1] = pack_bf16(p0, p1);
+                dd[e >> 1] = pack_bf16(ds.x, ds.y);
+            }
+        }
+        // P^T and dS^T (8 columns per half) into the first 16 columns of this
+        // chunk's own S^T / dP^T columns
+        tmem_st8(tm + kColS + c * 32 + hf * 8, pp);
+        tmem_st8(tm + kColDP + c * 32 + hf * 8, dd);
+        // dS row (this key) for these 16 queries: 2 chunks of 16 bytes, 128-byte swizzle
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int chunk = h * 4 + hf * 2 + u;
+            uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (krow & 7)) << 4)) = v;
+        }
+        if (hf == 1) {
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_pch + 8u * (uint32_t)c);
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -282,63 +351,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 }
                 tc_fence_after();
                 const bool edge = (i0 == item.j0) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = 2 * grp + h;
-                    // the chunk's 32 queries in two halves of 16 columns (keeps the live
-                    // registers low enough for the compiler to interleave the pairs)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int col = c * 32 + hf * 16;
-                        uint32_t sr[16], dr[16];
-                        tmem_ld16(tmem + lane_addr + kColS + col, sr);
-                        tmem_ld16(tmem + lane_addr + kColDP + col, dr);
-                        tmem_ld_wait();
-                        const float4* nl4 = reinterpret_cast<const float4*>(s_nl + col);
-                        const float4* nd4 = reinterpret_cast<const float4*>(s_nd + col);
-                        uint32_t pp[8], dd[8];
-#pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            const float4 L4 = nl4[e4], D4 = nd4[e4];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int e = 4 * e4 + 2 * u;
-                                const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
-                                const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
-                                const float2 x = ffma2(
-                                    make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nl);
-                                float p0 = ex2(x.x), p1 = ex2(x.y);
-                                if (edge) {
-                                    const int q = i0 + col + e;
-                                    const bool key_ok = key < item.j1;
-                                    p0 = (key_ok && key <= q && q < item.q_end) ? p0 : 0.f;
-                                    p1 = (key_ok && key <= q + 1 && q + 1 < item.q_end) ? p1 : 0.f;
-                                }
-                                const float2 dpv = fadd2(
-                                    make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd);
-                                const float2 ds = fmul2(make_float2(p0, p1), dpv);
-                                pp[e >> 1] = pack_bf16(p0, p1);
-                                dd[e >> 1] = pack_bf16(ds.x, ds.y);
-                            }
-                        }
-                        // P^T and dS^T (8 columns per half) into the first 16 columns of
-                        // this chunk's own S^T / dP^T columns
-                        tmem_st8(tmem + lane_addr + kColS + c * 32 + hf * 8, pp);
-                        tmem_st8(tmem + lane_addr + kColDP + c * 32 + hf * 8, dd);
-                        // dS row (this key) for these 16 queries: 2 chunks of 16 bytes,
-                        // 128-byte swizzle
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int chunk = h * 4 + hf * 2 + u;
-                            uint4 v = make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-                            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (krow & 7)) << 4)) = v;
-                        }
-                    }
-                    tmem_st_wait();
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(bar(LY::B_PCH + c));
-                }
+                if (edge)
+                    sg_block<true>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
+                else
+                    sg_block<false>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
             }
             if (!ok) break;
             // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16)
