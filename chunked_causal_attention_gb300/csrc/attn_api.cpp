@@ -2,6 +2,7 @@
 // kernel launches and status read-back. No device memory is allocated here.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -141,6 +142,20 @@ void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
     L.bytes = L.off_dq + round_up((size_t)BH * g.T * g.D * sizeof(float), kAlign);
 }
 
+}  // namespace
+
+void attn::wait_settings(uint64_t* wait_ns, int32_t* stall) {
+    *wait_ns = 4000000000ull;
+    *stall = 0;
+    if (const char* e = std::getenv("ATTN_WAIT_LIMIT_MS")) {
+        long v = std::strtol(e, nullptr, 10);
+        if (v > 0 && v <= 600000) *wait_ns = (uint64_t)v * 1000000ull;
+    }
+    if (const char* e = std::getenv("ATTN_TEST_STALL_PRODUCER")) *stall = std::atoi(e) != 0;
+}
+
+namespace {
+
 int upload(void* dst, const void* src, size_t bytes, cudaStream_t s) {
     if (!bytes) return ATTN_OK;
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess ? ATTN_OK : ATTN_E_CUDA;
@@ -192,6 +207,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
             a.items = (const FwdItem*)(w + L.off_items);
             a.n_items = (int32_t)L.items.size();
             a.group = kGroupFwd;
+            wait_settings(&a.wait_ns, &a.stall);
             a.g = g;
             if ((st = launched(launch_fwd_tiles_tc(a, s)))) return st;
         }
@@ -243,6 +259,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
         a.items = (const BwdItem*)(w + L.off_items);
         a.n_items = (int32_t)L.items.size();
         a.group = kGroupBwd;
+        wait_settings(&a.wait_ns, &a.stall);
         a.g = g;
         if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
     }

@@ -64,6 +64,8 @@ struct FwdArgs {
     const FwdItem* items;
     int32_t n_items;
     int32_t group;        // items per head group in the work order
+    uint64_t wait_ns;     // limit of every mbarrier wait
+    int32_t stall;        // test only: the TMA producer issues nothing
     Geom g;
 };
 
@@ -91,8 +93,15 @@ struct BwdArgs {
     const BwdItem* items;
     int32_t n_items;
     int32_t group;
+    uint64_t wait_ns;     // limit of every mbarrier wait
+    int32_t stall;        // test only: the TMA producer issues nothing
     Geom g;
 };
+
+// Wait limit and producer stall for the tile kernels, from the environment:
+// ATTN_WAIT_LIMIT_MS (default 4000) and ATTN_TEST_STALL_PRODUCER (default 0,
+// used by the failure-detection test to make every wait run out).
+void wait_settings(uint64_t* wait_ns, int32_t* stall);
 
 struct DqArgs {
     const float* dq_acc;

@@ -45,7 +45,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColDP = 128;
 constexpr uint32_t kColDV = 256;
-constexpr uint64_t kWaitNs = 4000000000ull;
 
 template <int D>
 struct BwdTcLayout {
@@ -209,12 +208,12 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tma_prefetch_desc(&tmdo);
             uint32_t qc = 0, ic = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+            for (int w = blockIdx.x; w < n_work && !a.stall && ok && !*abort_flag; w += gridDim.x, ++ic) {
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const BwdItem item = a.items[it];
                 const int b = bh / a.g.H, h = bh % a.g.H;
-                ok = mbar_wait(bar(LY::B_KVEMPTY), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_KVEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 mbar_expect_tx(bar(LY::B_KVFULL), 2 * LY::TILE);
                 load_tile_b<D>(sbase + LY::K_OFF, &tmk, bar(LY::B_KVFULL), mp, item.j0, h, b);
@@ -222,7 +221,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 const int nq = (item.q_end - item.j0 + 127) / 128;
                 for (int i = 0; i < nq; ++i, ++qc) {
                     const uint32_t s = qc & 1;
-                    ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_QFULL + s), LY::STAGE);
                     const int row = item.j0 + (nq - 1 - i) * 128;
@@ -246,12 +245,12 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const BwdItem item = a.items[it];
                 const int nq = (item.q_end - item.j0 + 127) / 128;
-                ok = mbar_wait(bar(LY::B_KVFULL), ic & 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_KVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 for (int i = 0; i < nq; ++i, ++qc, ++gb) {
                     const uint32_t s = qc & 1;
-                    ok = mbar_wait(bar(LY::B_QFULL + s), (qc >> 1) & 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_QFULL + s), (qc >> 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t q0 = sbase + LY::QDO_OFF + s * LY::STAGE;
@@ -263,7 +262,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                                kk > 0);
                     }
                     if (gb > 0) {
-                        ok = mbar_wait(bar(LY::B_DQFREE), (gb - 1) & 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_DQFREE), (gb - 1) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
                     }
@@ -275,14 +274,14 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     }
                     mma_commit(bar(LY::B_SDP));
                     if (i == 0) {
-                        ok = mbar_wait(bar(LY::B_DKDVFREE), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_DKDVFREE), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                     }
                     // dV += P^T dO and dK += dS^T Q one 32-query chunk (two k-steps) at a
                     // time, in the order the two softmax-gradient groups release them
                     for (int n = 0; n < 4 && ok; ++n) {
                         const int c = (n & 1) * 2 + (n >> 1);     // 0, 2, 1, 3
-                        ok = mbar_wait(bar(LY::B_PCH + c), gb & 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_PCH + c), gb & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
@@ -338,15 +337,19 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             }
             for (int i = 0; i < nq; ++i, ++gb) {
                 const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
                 named_sync(1 + grp, 128);
                 *stage_dst = next * mul;
                 named_sync(1 + grp, 128);
                 if (i + 1 < nq) next = src[i0 - 128 + 64 * grp + (krow & 63)];
-                ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 if (gb > 0) {
                     // dS in shared memory is free once dQ of the previous block has completed
-                    ok = mbar_wait(bar(LY::B_DQFULL), (gb - 1) & 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_DQFULL), (gb - 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                 }
                 tc_fence_after();
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             }
             if (!ok) break;
             // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16)
-            ok = mbar_wait(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, kWaitNs);
+            ok = mbar_wait(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
             if (!ok) break;
             tc_fence_after();
             const int b_ = bh / a.g.H, h_ = bh % a.g.H;
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 const int i0 = item.j0 + (nq - 1 - i) * 128;
                 const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
                 uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
-                ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32
@@ -428,6 +431,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     }
                 }
                 fence_proxy_async_smem();
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
                 named_sync(3, 128);
                 if (qrow == 0) {
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             if (elect_one()) {
                 mma_commit(bar(LY::B_DRAIN));
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(bar(LY::B_DRAIN), 0) && globaltimer() - t0 < kWaitNs) {
+                while (!mbar_try_wait(bar(LY::B_DRAIN), 0) && globaltimer() - t0 < a.wait_ns) {
                 }
             }
             __syncwarp();

@@ -38,7 +38,6 @@ constexpr int KV_STAGES = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
-constexpr uint64_t kWaitNs = 4000000000ull;    // 4 s per wait: far above any legitimate wait
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 template <int D>
@@ -132,12 +131,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             uint32_t kc = 0, vc = 0, ic = 0;
-            for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x, ++ic) {
+            for (int w = blockIdx.x; w < n_work && !a.stall && !*abort_flag; w += gridDim.x, ++ic) {
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
                 const int b = bh / a.g.H, h = bh % a.g.H;
-                if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs)) break;
+                if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns)) break;
                 mbar_expect_tx(bar(LY::B_QFULL), LY::TILE);
                 load_tile<D>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
                 const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
@@ -145,12 +144,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int j = 0; j < nblk && ok; ++j) {
                     const int row = item.kv_lo + j * 128;
                     const uint32_t ks = kc % KV_STAGES, vs = vc % KV_STAGES;
-                    ok = mbar_wait(bar(LY::B_KEMPTY + ks), ((kc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_KEMPTY + ks), ((kc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_KFULL + ks), LY::TILE);
                     load_tile<D>(sbase + LY::K_OFF + ks * LY::TILE, &tmk, bar(LY::B_KFULL + ks), mp, row, h, b);
                     ++kc;
-                    ok = mbar_wait(bar(LY::B_VEMPTY + vs), ((vc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_VEMPTY + vs), ((vc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE);
                     load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mp, row, h, b);
@@ -171,7 +170,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
                 const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
-                ok = mbar_wait(bar(LY::B_QFULL), ic & 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_QFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t q0 = sbase + LY::Q_OFF;
@@ -180,7 +179,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (j < nblk) {
                         // S_j = Q K_j^T into S buffer (gt + j) & 1
                         const uint32_t ks = kc % KV_STAGES;
-                        ok = mbar_wait(bar(LY::B_KFULL + ks), (kc / KV_STAGES) & 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_KFULL + ks), (kc / KV_STAGES) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t k0 = sbase + LY::K_OFF + ks * LY::TILE;
@@ -200,13 +199,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t t = gt + j - 1;
                         const uint32_t pb = t & 1;
                         if (j == 1) {
-                            ok = mbar_wait(bar(LY::B_OFREE), (ic & 1) ^ 1, abort_flag, a.status, kWaitNs);
+                            ok = mbar_wait(bar(LY::B_OFREE), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                             if (!ok) break;
                         }
-                        ok = mbar_wait(bar(LY::B_PFULL + pb), (t >> 1) & 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_PFULL + pb), (t >> 1) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         const uint32_t vs = pv_vc % KV_STAGES;
-                        ok = mbar_wait(bar(LY::B_VFULL + vs), (pv_vc / KV_STAGES) & 1, abort_flag, a.status, kWaitNs);
+                        ok = mbar_wait(bar(LY::B_VFULL + vs), (pv_vc / KV_STAGES) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t v0 = sbase + LY::V_OFF + vs * LY::TILE;
@@ -241,7 +240,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nblk && ok; ++j) {
                 const uint32_t t = gt + j, b = t & 1;
-                ok = mbar_wait(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, kWaitNs);
+                ok = mbar_wait(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_addr + kColS + b * 128;
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // tcgen05.ld/st are warp-collective: rescale O if any row of the warp needs it
                 if (__any_sync(0xffffffffu, rescale) && j > 0) {
                     // O holds the sum over tiles < j once PV_{j-1} has completed
-                    ok = mbar_wait(bar(LY::B_ODONE), (t - 1) & 1, abort_flag, a.status, kWaitNs);
+                    ok = mbar_wait(bar(LY::B_ODONE), (t - 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t oa = tmem + lane_addr + kColO;
@@ -327,7 +326,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // epilogue: wait for the last PV of the item, then O / l. This uses the
             // once-per-item barrier: when the softmax warps get here up to two PVs
             // may still be in flight, more than a per-PV parity wait can tell apart.
-            ok = mbar_wait(bar(LY::B_OFULL), ic & 1, abort_flag, a.status, kWaitNs);
+            ok = mbar_wait(bar(LY::B_OFULL), ic & 1, abort_flag, a.status, a.wait_ns);
             if (!ok) break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -392,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (elect_one()) {
                 mma_commit(bar(LY::B_DRAIN));
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(bar(LY::B_DRAIN), 0) && globaltimer() - t0 < kWaitNs) {
+                while (!mbar_try_wait(bar(LY::B_DRAIN), 0) && globaltimer() - t0 < a.wait_ns) {
                 }
             }
             __syncwarp();

@@ -1,0 +1,63 @@
+"""Failure detection without a GPU fault: every mbarrier wait in the tile kernels
+is bounded. With the test-only producer stall (ATTN_TEST_STALL_PRODUCER=1) no
+tile is ever loaded, so every wait runs out after ATTN_WAIT_LIMIT_MS; the
+kernels record ATTN_E_TIMEOUT in the workspace status word, release TMEM and
+return. The host reads the status, and the same CUDA context then runs a
+normal forward and backward that match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_causal_attention_gb300 as cca
+from chunked_causal_attention_gb300.workloads import make_inputs
+from oracle import attention as A
+from oracle import plan as P
+
+from parity import check_fwd, check_grad, default_scale, head, lse_head
+
+pytestmark = pytest.mark.gpu
+
+ATTN_E_TIMEOUT = 6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    if not os.path.exists(cca._lib.LIB_PATH):
+        from chunked_causal_attention_gb300 import build
+        build.build()
+
+
+def test_stalled_producer_times_out_and_context_survives(monkeypatch):
+    L, H, D = 2048, 2, 128
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=88))
+    chunks = P.plan(L, 2, P.FLOPS)
+    shape = cca.shape_of(q)
+    o, lse = torch.zeros_like(q), torch.zeros(1, H, L, device="cuda")
+    dq, dk, dv = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
+    ws_f = cca.workspace(shape, chunks, 0)
+    ws_b = cca.workspace(shape, chunks, 1)
+
+    monkeypatch.setenv("ATTN_WAIT_LIMIT_MS", "200")
+    monkeypatch.setenv("ATTN_TEST_STALL_PRODUCER", "1")
+    cca.attn_fwd(q, k, v, chunks, shape, o, lse, ws_f)          # enqueues and returns ATTN_OK
+    assert cca.attn_status(ws_f) == ATTN_E_TIMEOUT
+    assert cca.attn_status(ws_f) == 0                           # read clears the word
+    cca.attn_bwd(q, k, v, o, lse, do, chunks, shape, dq, dk, dv, ws_b)
+    assert cca.attn_status(ws_b) == ATTN_E_TIMEOUT
+
+    monkeypatch.delenv("ATTN_TEST_STALL_PRODUCER")
+    monkeypatch.delenv("ATTN_WAIT_LIMIT_MS")
+    o, lse = cca.forward(q, k, v, chunks)
+    dq, dk, dv = cca.backward(q, k, v, o, lse, do, chunks)
+    torch.cuda.synchronize()
+    sc = default_scale(D)
+    for h in range(H):
+        qh, kh, vh, doh = (head(x, 0, h, False) for x in (q, k, v, do))
+        rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, sc)
+        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"after timeout h{h}")
+        check_grad(head(dq, 0, h, False), rdq, f"after timeout dQ h{h}")
+        check_grad(head(dk, 0, h, False), rdk, f"after timeout dK h{h}")
+        check_grad(head(dv, 0, h, False), rdv, f"after timeout dV h{h}")
