@@ -301,6 +301,35 @@ def chunked_forward(q, k, v, chunks: Sequence[Tuple[int, int, int, int]], scale:
     return O, LSE
 
 
+def chunk_backward(q, k, v, do, qb: int, qe: int, cb: int, scale: float, row_block: int = 512):
+    """Contributions of the query rows of ONE chunk, [qb, qe) with context
+    starting at cb (the document start), to the gradients: the definition's
+    sums restricted to t in [qb, qe). Returns (dQ rows [qb, qe), dK and dV
+    contributions for keys [cb, qe)).
+
+    This is how the chunked method runs the backward (InfiniPipe §II-A: the
+    K/V gradients of a token gather contributions from all later tokens; SPPO
+    §5.1 keeps each subsequence's K/V resident for the later subsequences):
+    chunks are processed in reverse order and each chunk adds its queries'
+    share to the keys of its context. dQ of the chunk's rows is complete,
+    because every key a row can see lies in [cb, qe)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq = np.zeros((qe - qb, q.shape[1]))
+    dk = np.zeros((qe - cb, k.shape[1]))
+    dv = np.zeros((qe - cb, v.shape[1]))
+    for r0 in range(qb, qe, row_block):
+        r1 = min(r0 + row_block, qe)
+        P, _ = _softmax_rows(_score_rows(q, k, scale, r0, r1, cb))   # keys [cb, r1)
+        o = P @ v[cb:r1]
+        D = np.sum(do[r0:r1] * o, axis=1, keepdims=True)
+        dP = do[r0:r1] @ v[cb:r1].T
+        dS = P * (dP - D)
+        dq[r0 - qb:r1 - qb] = scale * (dS @ k[cb:r1])
+        dk[:r1 - cb] += scale * (dS.T @ q[r0:r1])
+        dv[:r1 - cb] += P.T @ do[r0:r1]
+    return dq, dk, dv
+
+
 def causal_flops(pairs: int, D: int) -> Tuple[int, int]:
     """Algorithmic FLOPs of (forward, backward) for ``pairs`` visible (t, j)
     pairs: 2 GEMMs forward (QK^T, PV) and 5 backward (S, dP, dV, dK, dQ)."""

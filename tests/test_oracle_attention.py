@@ -247,3 +247,55 @@ def test_periodic_keys_closed_form_matches_definition(T, p, D):
     Op, Lp, dqp, dvp = A.periodic_keys(q, kc, v, do, sc)
     for a, b in ((Op, O), (Lp, L), (dqp, dq), (dvp, dv)):
         np.testing.assert_allclose(a, b, atol=1e-10, rtol=1e-10)
+
+
+# ---------------------------------------------------- chunk-streamed backward
+
+def torch_chunk_grads(q, k, v, do, qb, qe, cb, sc):
+    """Library pin: torch float64 autograd of sum(dO . O) over the chunk's rows
+    only, O from an explicitly masked softmax of the chunk's queries against
+    its context keys [cb, qe)."""
+    Q = torch.tensor(q[qb:qe], dtype=torch.float64, requires_grad=True)
+    K = torch.tensor(k[cb:qe], dtype=torch.float64, requires_grad=True)
+    V = torch.tensor(v[cb:qe], dtype=torch.float64, requires_grad=True)
+    t = torch.arange(qb, qe)[:, None]
+    j = torch.arange(cb, qe)[None, :]
+    S = (Q @ K.T) * sc
+    S = S.masked_fill(j > t, float("-inf"))
+    O = torch.softmax(S, dim=-1) @ V
+    (O * torch.tensor(do[qb:qe], dtype=torch.float64)).sum().backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+@pytest.mark.parametrize("qb,qe,cb", [(0, 96, 0), (130, 257, 0), (300, 301, 0), (170, 300, 100)])
+def test_chunk_backward_matches_autograd(qb, qe, cb):
+    T, D, sc = 301, 8, 0.35
+    q, k, v, do = (rand((T, D), s) for s in (81, 82, 83, 84))
+    dq, dk, dv = A.chunk_backward(q, k, v, do, qb, qe, cb, sc, row_block=40)
+    tq, tk, tv = torch_chunk_grads(q, k, v, do, qb, qe, cb, sc)
+    np.testing.assert_allclose(dq, tq, atol=1e-11)
+    np.testing.assert_allclose(dk, tk, atol=1e-11)
+    np.testing.assert_allclose(dv, tv, atol=1e-11)
+
+
+@pytest.mark.parametrize("mode", [P.UNIFORM, P.FLOPS, P.FLOPS_RESPLIT_EDGES])
+def test_chunk_backward_streamed_equals_full(mode):
+    """Chunks processed in reverse order: summed contributions equal the
+    plain backward, and after chunk c has run, the keys of chunk c hold their
+    final gradients (later chunks have all contributed already)."""
+    T, D, sc = 1000, 16, 0.25
+    for docs, chunks in (([0, T], P.plan(T, 4, mode)),
+                         ([0, 3, 3, 410, 411, T], P.plan_varlen([0, 3, 3, 410, 411, T], 200, mode))):
+        q, k, v, do = (rand((T, D), s) for s in (91, 92, 93, 94))
+        dq, dk, dv, _, _ = A.backward(q, k, v, do, sc, docs)
+        adk, adv, gq = np.zeros_like(dk), np.zeros_like(dv), np.zeros_like(dq)
+        for qb, qe, cb, _m in reversed(chunks):
+            cq, ck, cv = A.chunk_backward(q, k, v, do, qb, qe, cb, sc)
+            gq[qb:qe] = cq
+            adk[cb:qe] += ck
+            adv[cb:qe] += cv
+            np.testing.assert_allclose(adk[qb:qe], dk[qb:qe], atol=1e-12)
+            np.testing.assert_allclose(adv[qb:qe], dv[qb:qe], atol=1e-12)
+        np.testing.assert_allclose(gq, dq, atol=1e-12)
+        np.testing.assert_allclose(adk, dk, atol=1e-12)
+        np.testing.assert_allclose(adv, dv, atol=1e-12)
