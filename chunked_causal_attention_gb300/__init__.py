@@ -10,22 +10,28 @@ from __future__ import annotations
 
 from typing import Optional, Sequence
 
-from ._lib import (AttnError, EXPORTS, PLAN_FLOPS, PLAN_FLOPS_RESPLIT_EDGES, PLAN_UNIFORM, attn_bwd,
-                   attn_bwd_dq, attn_bwd_prep, attn_bwd_tiles, attn_fwd, attn_fwd_merge, attn_fwd_tiles,
-                   attn_plan, attn_plan_varlen, attn_shape, attn_status, attn_workspace_size, lib, make_shape,
-                   shape_of, strerror, version)
+from ._lib import (AttnError, EXPORTS, PASS_BWD, PASS_BWD_CHUNK, PASS_FWD, PLAN_FLOPS, PLAN_FLOPS_RESPLIT_EDGES,
+                   PLAN_UNIFORM, attn_bwd, attn_bwd_chunk, attn_bwd_dq, attn_bwd_prep, attn_bwd_tiles, attn_fwd,
+                   attn_fwd_merge, attn_fwd_tiles, attn_plan, attn_plan_varlen, attn_shape, attn_status,
+                   attn_workspace_size, lib, make_shape, shape_of, strerror, version)
 
 __all__ = ["AttnError", "EXPORTS", "PLAN_UNIFORM", "PLAN_FLOPS", "PLAN_FLOPS_RESPLIT_EDGES", "attn_plan",
            "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles", "attn_fwd_merge", "attn_bwd",
-           "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_status", "attn_shape", "make_shape",
-           "shape_of", "workspace", "forward", "backward", "lib", "strerror", "version"]
+           "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_bwd_chunk", "attn_status", "attn_shape",
+           "make_shape", "shape_of", "workspace", "forward", "backward", "forward_streamed", "backward_streamed",
+           "PASS_FWD", "PASS_BWD", "PASS_BWD_CHUNK", "lib", "strerror", "version"]
 
 
-def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda"):
+def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", per_chunk: bool = False):
     """A uint8 device buffer of the size the library asks for (pass 0 forward,
-    1 backward), with its 256-byte status header zeroed."""
+    1 backward, 2 backward of one chunk), with its 256-byte status header
+    zeroed. per_chunk (always for pass 2): large enough for a call on any one
+    of the chunks alone."""
     import torch
-    n = attn_workspace_size(shape, chunks, pass_)
+    if per_chunk or pass_ == PASS_BWD_CHUNK:
+        n = max(attn_workspace_size(shape, [c], pass_) for c in chunks)
+    else:
+        n = attn_workspace_size(shape, chunks, pass_)
     ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
     ws[:256].zero_()
     return ws
@@ -53,3 +59,33 @@ def backward(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = N
         ws = workspace(shape, chunks, 1, q.device)
     attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream)
     return dq, dk, dv
+
+
+def forward_streamed(q, k, v, chunks: Sequence, scale: Optional[float] = None, packed: bool = False, stream=None):
+    """The forward one chunk at a time, in chunk order: each call computes one
+    chunk's rows against the keys before it, which are resident in k, v."""
+    import torch
+    shape = shape_of(q, scale, packed)
+    o = torch.empty_like(q)
+    lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
+    ws = workspace(shape, chunks, PASS_FWD, q.device, per_chunk=True)
+    for c in chunks:
+        attn_fwd(q, k, v, [c], shape, o, lse, ws, stream)
+    return o, lse
+
+
+def backward_streamed(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = None, packed: bool = False,
+                      stream=None):
+    """The backward one chunk at a time, in reverse chunk order, with fp32
+    dK/dV accumulators shared by the calls (attn_bwd_chunk). Returns
+    (dq, dk, dv, dk_acc, dv_acc)."""
+    import torch
+    shape = shape_of(q, scale, packed)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # fp32 accumulators at the same element offsets as k and v
+    dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=k.device).zero_()
+    dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=v.device).zero_()
+    ws = workspace(shape, chunks, PASS_BWD_CHUNK, q.device)
+    for c in reversed(list(chunks)):
+        attn_bwd_chunk(q, k, v, o, lse, dout, c, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream)
+    return dq, dk, dv, dk_acc, dv_acc

@@ -26,7 +26,12 @@ PLAN_FLOPS_RESPLIT_EDGES = 2
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
-           "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
+           "attn_bwd_chunk", "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
+
+# attn_workspace_size passes
+PASS_FWD = 0
+PASS_BWD = 1
+PASS_BWD_CHUNK = 2
 
 # Size of the library-held scratch area of attn_fwd_noalloc (ATTN_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -69,6 +74,8 @@ _SIG = {
     "attn_bwd_tiles": ([_VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
                        ctypes.c_int),
     "attn_bwd_dq": ([_CP, _I32, _SP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
+    "attn_bwd_chunk": ([_VP, _VP, _VP, _VP, _VP, _VP, _CP, _SP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
+                       ctypes.c_int),
     "attn_fwd_noalloc": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP], ctypes.c_int),
     "attn_status": ([_VP, _VP], ctypes.c_int),
     "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -216,6 +223,15 @@ def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
     arr, n = chunk_array(chunks)
     _check("attn_bwd_dq", lib().attn_bwd_dq(arr, n, ctypes.byref(shape), _ptr(dq), _ptr(ws),
                                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def attn_bwd_chunk(q, k, v, o, lse, dout, chunk, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream=None) -> None:
+    """Backward of one chunk's rows (chunk-streamed; see include/attn.h)."""
+    arr, n = chunk_array([chunk])
+    _check("attn_bwd_chunk", lib().attn_bwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr,
+                                                  ctypes.byref(shape), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk_acc),
+                                                  _ptr(dv_acc), _ptr(ws), ws.numel() * ws.element_size(),
+                                                  _stream(stream)))
 
 
 def attn_fwd_noalloc(q, k, v, chunks, shape, o, lse, stream=None) -> None:

@@ -118,11 +118,25 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
 // --------------------------------------------------------------- backward layout
 struct BwdLayout {
     std::vector<BwdItem> items;
+    int32_t row0, rows;   // token rows held by delta and the dQ accumulator
     size_t off_items, off_delta, off_dq, bytes;
 };
 
-void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
+void bwd_finish_layout(const Geom& g, BwdLayout& L) {
     const int64_t BH = (int64_t)g.B * g.H;
+    // heaviest first: most query blocks
+    std::stable_sort(L.items.begin(), L.items.end(), [](const BwdItem& a, const BwdItem& b) {
+        return (a.q_end - a.q_lo) > (b.q_end - b.q_lo);
+    });
+    L.off_items = kHeaderBytes;
+    L.off_delta = L.off_items + round_up(L.items.size() * sizeof(BwdItem), kAlign);
+    L.off_dq = L.off_delta + round_up((size_t)BH * L.rows * sizeof(float), kAlign);
+    L.bytes = L.off_dq + round_up((size_t)BH * L.rows * g.D * sizeof(float), kAlign);
+}
+
+// Whole backward: one item per key tile of every document; the tile's
+// queries run from its first key to the document end.
+void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
     L.items.clear();
     int32_t i = 0;
     while (i < n) {
@@ -130,16 +144,24 @@ void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
         int32_t j = i + 1;
         while (j < n && c[j].ctx_begin == s) { e = c[j].q_end; ++j; }
         for (int32_t j0 = s; j0 < e; j0 += kTile)
-            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, e), e, s});
+            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, e), e, j0});
         i = j;
     }
-    std::stable_sort(L.items.begin(), L.items.end(), [](const BwdItem& a, const BwdItem& b) {
-        return (a.q_end - a.j0) > (b.q_end - b.j0);
-    });
-    L.off_items = kHeaderBytes;
-    L.off_delta = L.off_items + round_up(L.items.size() * sizeof(BwdItem), kAlign);
-    L.off_dq = L.off_delta + round_up((size_t)BH * g.T * sizeof(float), kAlign);
-    L.bytes = L.off_dq + round_up((size_t)BH * g.T * g.D * sizeof(float), kAlign);
+    L.row0 = 0;
+    L.rows = g.T;
+    bwd_finish_layout(g, L);
+}
+
+// Backward of one chunk: one item per key tile of the chunk's context
+// [ctx_begin, q_end); a tile's queries are the chunk's rows at or after its
+// first key. delta and dQ cover the chunk's rows only.
+void bwd_chunk_layout(const Geom& g, const attn_chunk& c, BwdLayout& L) {
+    L.items.clear();
+    for (int32_t j0 = c.ctx_begin; j0 < c.q_end; j0 += kTile)
+        L.items.push_back(BwdItem{j0, std::min(j0 + kTile, c.q_end), c.q_end, std::max(j0, c.q_begin)});
+    L.row0 = c.q_begin;
+    L.rows = c.q_end - c.q_begin;
+    bwd_finish_layout(g, L);
 }
 
 }  // namespace
@@ -227,6 +249,42 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
 
 enum BwdStage { kPrep = 1, kTiles = 2, kDq = 4 };
 
+// Enqueue the stages of a backward laid out in L. dk_acc/dv_acc non-null:
+// chunk-streamed epilogue (fp32 accumulation, bf16 from key emit_from on).
+int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, const void* v, const void* o,
+               const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dk_acc, float* dv_acc,
+               int32_t emit_from, void* ws, cudaStream_t s, int stages) {
+    int st;
+    uint8_t* w = (uint8_t*)ws;
+    float* delta = (float*)(w + L.off_delta);
+    float* dq_acc = (float*)(w + L.off_dq);
+    if (stages & kPrep) {
+        if ((st = reset_header(ws, s))) return st;
+        PrepArgs a{o, dout, delta, dq_acc, L.row0, L.rows, g};
+        if ((st = launched(launch_bwd_prep(a, s)))) return st;
+    }
+    if (stages & kTiles) {
+        if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) return st;
+        BwdArgs a;
+        a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
+        a.dk = dk; a.dv = dv; a.dq_acc = dq_acc;
+        a.row0 = L.row0; a.rows = L.rows;
+        a.dk_acc = dk_acc; a.dv_acc = dv_acc; a.emit_from = emit_from;
+        a.status = (uint32_t*)ws;
+        a.items = (const BwdItem*)(w + L.off_items);
+        a.n_items = (int32_t)L.items.size();
+        a.group = kGroupBwd;
+        wait_settings(&a.wait_ns, &a.stall);
+        a.g = g;
+        if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
+    }
+    if (stages & kDq) {
+        DqArgs a{dq_acc, dq, L.row0, L.rows, g};
+        if ((st = launched(launch_bwd_dq(a, s)))) return st;
+    }
+    return ATTN_OK;
+}
+
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cudaStream_t s, int stages) {
@@ -243,31 +301,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
     BwdLayout L;
     bwd_layout(g, chunks, n, L);
     if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
-    uint8_t* w = (uint8_t*)ws;
-    float* delta = (float*)(w + L.off_delta);
-    float* dq_acc = (float*)(w + L.off_dq);
-    if (stages & kPrep) {
-        if ((st = reset_header(ws, s))) return st;
-        PrepArgs a{o, dout, delta, dq_acc, g};
-        if ((st = launched(launch_bwd_prep(a, s)))) return st;
-    }
-    if (stages & kTiles) {
-        if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) return st;
-        BwdArgs a;
-        a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
-        a.dk = dk; a.dv = dv; a.dq_acc = dq_acc; a.status = (uint32_t*)ws;
-        a.items = (const BwdItem*)(w + L.off_items);
-        a.n_items = (int32_t)L.items.size();
-        a.group = kGroupBwd;
-        wait_settings(&a.wait_ns, &a.stall);
-        a.g = g;
-        if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
-    }
-    if (stages & kDq) {
-        DqArgs a{dq_acc, dq, g};
-        if ((st = launched(launch_bwd_dq(a, s)))) return st;
-    }
-    return ATTN_OK;
+    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, nullptr, nullptr, 0, ws, s, stages);
 }
 
 }  // namespace
@@ -289,6 +323,12 @@ int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32
         if ((st = check_chunks_bwd(chunks, n, g.T))) return st;
         BwdLayout L;
         bwd_layout(g, chunks, n, L);
+        *bytes = L.bytes;
+    } else if (pass == 2) {
+        if (n != 1) return ATTN_E_INVAL;
+        if ((st = check_chunks_fwd(chunks, n, g.T))) return st;
+        BwdLayout L;
+        bwd_chunk_layout(g, chunks[0], L);
         *bytes = L.bytes;
     } else {
         return ATTN_E_INVAL;
@@ -337,6 +377,25 @@ int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape, vo
                 size_t ws_bytes, void* stream) {
     return bwd_common(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, chunks, n, shape, dq, nullptr,
                       nullptr, ws, ws_bytes, (cudaStream_t)stream, kDq);
+}
+
+int attn_bwd_chunk(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, const attn_chunk* chunk, const attn_shape* shape, void* dq, void* dk,
+                   void* dv, float* dk_acc, float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
+    Geom g;
+    int st = check_shape(shape, &g);
+    if (st) return st;
+    if ((st = check_chunks_fwd(chunk, 1, g.T))) return st;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc};
+    for (const void* p : ptrs)
+        if (!p) return ATTN_E_INVAL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return ATTN_E_ALIGN;
+    BwdLayout L;
+    bwd_chunk_layout(g, *chunk, L);
+    if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
+    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc, chunk->q_begin, ws,
+                      (cudaStream_t)stream, kPrep | kTiles | kDq);
 }
 
 int attn_status(void* ws, void* stream) {

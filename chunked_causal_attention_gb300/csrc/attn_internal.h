@@ -41,12 +41,14 @@ struct MergeSeg {
 };
 static_assert(sizeof(MergeSeg) == 32, "MergeSeg layout");
 
-// One backward work item: keys [j0, j1) (j1 - j0 <= 128) of a document
-// that ends at q_end; queries [j0, q_end) see them.
+// One backward work item: keys [j0, j1) (j1 - j0 <= 128) of a document;
+// the queries [q_lo, q_end) are walked in blocks of 128 rows starting at
+// q_lo. Whole backward: q_lo = j0 and q_end = the document end. Backward of
+// one chunk [q_begin, q_end): q_lo = max(j0, q_begin).
 struct BwdItem {
     int32_t j0, j1;
     int32_t q_end;
-    int32_t doc_begin;
+    int32_t q_lo;
 };
 static_assert(sizeof(BwdItem) == 16, "BwdItem layout");
 
@@ -78,9 +80,12 @@ struct MergeArgs {
     Geom g;
 };
 
+// delta and the dQ accumulator hold rows [row0, row0 + rows) of every
+// (batch, head): delta[bh*rows + t - row0], dq_acc[(bh*rows + t - row0)*D + d].
 struct PrepArgs {
     const void* o; const void* dout;
     float* delta; float* dq_acc;
+    int32_t row0, rows;
     Geom g;
 };
 
@@ -89,6 +94,12 @@ struct BwdArgs {
     const float* lse; const float* delta;
     void* dk; void* dv;
     float* dq_acc;
+    int32_t row0, rows;   // rows of delta and dq_acc (layout as PrepArgs)
+    // Chunk-streamed backward: fp32 dK/dV accumulators (element offsets of the
+    // bf16 tensors); the epilogue adds into them and writes bf16 dk/dv only for
+    // keys >= emit_from. Null for the whole backward (bf16 written directly).
+    float* dk_acc; float* dv_acc;
+    int32_t emit_from;
     uint32_t* status;
     const BwdItem* items;
     int32_t n_items;
@@ -104,8 +115,9 @@ struct BwdArgs {
 void wait_settings(uint64_t* wait_ns, int32_t* stall);
 
 struct DqArgs {
-    const float* dq_acc;
+    const float* dq_acc;  // rows [row0, row0 + rows) as PrepArgs
     void* dq;
+    int32_t row0, rows;
     Geom g;
 };
 
@@ -118,9 +130,9 @@ struct TcMaps {
 // dim, axes 1..3 are token/head/batch sorted by stride; box = 64 elements
 // (128 bytes, 128-byte swizzle) x 128 tokens. Fills `mp`. False on failure.
 bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
-// Rank-3 TMA map of the fp32 dQ accumulator [B*H][T][D]: box of 32 floats
+// Rank-3 TMA map of the fp32 dQ accumulator [B*H][rows][D]: box of 32 floats
 // (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
-bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g);
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);
 int device_sm_count();
 
 // Kernel launchers (return the launch error).

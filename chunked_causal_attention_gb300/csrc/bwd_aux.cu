@@ -2,7 +2,9 @@
 //   prep: D_t = sum_d dO_td * O_td in fp32 (the row term of dS = P o (dP - D)),
 //         and zeroing of the fp32 dQ accumulator.
 //   dq:   dQ = bf16(fp32 accumulator), written with the caller's strides.
-// One warp per (batch*head, token).
+// One warp per (batch*head, token) of the rows [row0, row0 + rows) the
+// workspace holds (all tokens for the whole backward, one chunk's rows for
+// the chunk-streamed backward).
 #include "device_common.cuh"
 
 namespace attn {
@@ -14,9 +16,9 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
     constexpr int PER = D / 32;
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int64_t total = (int64_t)a.g.B * a.g.H * a.g.T;
+    const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
-    const int bh = (int)(w / a.g.T), t = (int)(w % a.g.T);
+    const int bh = (int)(w / a.rows), t = a.row0 + (int)(w % a.rows);
     const int b = bh / a.g.H, h = bh % a.g.H;
     const int64_t off = (int64_t)b * a.g.sb + (int64_t)h * a.g.sh + (int64_t)t * a.g.st + lane * PER;
     const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o) + off;
@@ -44,9 +46,9 @@ __global__ void __launch_bounds__(256) dq_kernel(DqArgs a) {
     constexpr int PER = D / 32;
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int64_t total = (int64_t)a.g.B * a.g.H * a.g.T;
+    const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
-    const int bh = (int)(w / a.g.T), t = (int)(w % a.g.T);
+    const int bh = (int)(w / a.rows), t = a.row0 + (int)(w % a.rows);
     const int b = bh / a.g.H, h = bh % a.g.H;
     const float* src = a.dq_acc + w * D + lane * PER;
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +
@@ -58,7 +60,8 @@ __global__ void __launch_bounds__(256) dq_kernel(DqArgs a) {
 }  // namespace
 
 cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
-    const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.g.T + 7) / 8;
+    const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.rows + 7) / 8;
+    if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     if (a.g.D == 128)
         prep_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(a);
@@ -68,7 +71,8 @@ cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
-    const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.g.T + 7) / 8;
+    const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.rows + 7) / 8;
+    if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     if (a.g.D == 128)
         dq_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(a);

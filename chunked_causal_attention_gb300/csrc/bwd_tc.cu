@@ -1,12 +1,15 @@
 // Backward key-tile kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // One work item = 128 keys [j0, j1) of one (batch, head); the item walks the
-// query blocks of 128 rows that can see those keys (queries t >= j0 up to the
-// document end) from the last block down to the diagonal one: a key's dK/dV
-// collect the contributions of every later token of its sequence (InfiniPipe
-// §II-A: K/V gradients of a token depend on all subsequent tokens). Persistent
-// CTAs take items head-major (all CTAs on one head at a time), so the head's
-// Q/dO tiles and dQ accumulator rows are reused from L2.
+// query blocks of 128 rows [q_lo, q_end) that can see those keys from the last
+// block down to the first: a key's dK/dV collect the contributions of every
+// later token of its sequence (InfiniPipe §II-A: K/V gradients of a token
+// depend on all subsequent tokens). For the whole backward q_lo = j0 and q_end
+// is the document end; for the backward of one chunk the queries are that
+// chunk's rows, and dK/dV are added into fp32 accumulators that the chunks of a
+// document share when run in reverse order. Persistent CTAs take items
+// head-major (all CTAs on one head at a time), so the head's Q/dO tiles and
+// dQ accumulator rows are reused from L2.
 //
 // Warp roles (16 warps):
 //   warp 0       TMA producer: K, V once per item; Q and dO of a query block into
@@ -218,13 +221,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 mbar_expect_tx(bar(LY::B_KVFULL), 2 * LY::TILE);
                 load_tile_b<D>(sbase + LY::K_OFF, &tmk, bar(LY::B_KVFULL), mp, item.j0, h, b);
                 load_tile_b<D>(sbase + LY::V_OFF, &tmv, bar(LY::B_KVFULL), mp, item.j0, h, b);
-                const int nq = (item.q_end - item.j0 + 127) / 128;
+                const int nq = (item.q_end - item.q_lo + 127) / 128;
                 for (int i = 0; i < nq; ++i, ++qc) {
                     const uint32_t s = qc & 1;
                     ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_QFULL + s), LY::STAGE);
-                    const int row = item.j0 + (nq - 1 - i) * 128;
+                    const int row = item.q_lo + (nq - 1 - i) * 128;
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
                     load_tile_b<D>(st, &tmq, bar(LY::B_QFULL + s), mp, row, h, b);
                     load_tile_b<D>(st + LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, h, b);
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const BwdItem item = a.items[it];
-                const int nq = (item.q_end - item.j0 + 127) / 128;
+                const int nq = (item.q_end - item.q_lo + 127) / 128;
                 ok = mbar_wait(bar(LY::B_KVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
@@ -324,19 +327,20 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             int32_t it, bh;
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const BwdItem item = a.items[it];
-            const int nq = (item.q_end - item.j0 + 127) / 128;
+            const int nq = (item.q_end - item.q_lo + 127) / 128;
             const int key = item.j0 + krow;
-            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.g.T;
+            // src[t] for a token t: LSE (all tokens) or delta (rows [row0, row0 + rows))
+            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.rows - a.row0;
             const float mul = stage_l ? -kLog2e : -1.f;
             // raw value of the next block, scaled only when it is staged, so the
             // load's latency is not waited for until then
             float next = 0.f;
             {
-                const int q = item.j0 + (nq - 1) * 128 + 64 * grp + (krow & 63);
+                const int q = item.q_lo + (nq - 1) * 128 + 64 * grp + (krow & 63);
                 if (q < item.q_end) next = src[q];
             }
             for (int i = 0; i < nq; ++i, ++gb) {
-                const int i0 = item.j0 + (nq - 1 - i) * 128;   // query blocks walked from the last one down
+                const int i0 = item.q_lo + (nq - 1 - i) * 128;  // query blocks walked from the last one down
                 if (*abort_flag) {
                     ok = false;
                     break;
@@ -353,7 +357,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     if (!ok) break;
                 }
                 tc_fence_after();
-                const bool edge = (i0 == item.j0) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
+                // masks are needed where some key of the tile lies after some query of the
+                // block, where the block runs past the document or chunk end, and on a
+                // partial key tile
+                const bool edge = (i0 < item.j1 - 1) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
                 if (edge)
                     sg_block<true>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
                 else
@@ -370,21 +377,40 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const uint32_t col = grp == 0 ? kColDK : kColDV;
             const float gmul = grp == 0 ? a.g.scale : 1.f;
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(grp == 0 ? a.dk : a.dv) + roff;
+            // chunk-streamed backward: add into the fp32 accumulator row, and write
+            // bf16 only for the chunk's own keys (complete once their chunk has run)
+            float* acc = a.dk_acc ? (grp == 0 ? a.dk_acc : a.dv_acc) + roff : nullptr;
+            const bool emit = acc == nullptr || key >= a.emit_from;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_addr + col + c * 32, r);
                 tmem_ld_wait();
                 if (live) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                    float f[32];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * u + 0]) * gmul, __uint_as_float(r[8 * u + 1]) * gmul);
-                        v.y = pack_bf16(__uint_as_float(r[8 * u + 2]) * gmul, __uint_as_float(r[8 * u + 3]) * gmul);
-                        v.z = pack_bf16(__uint_as_float(r[8 * u + 4]) * gmul, __uint_as_float(r[8 * u + 5]) * gmul);
-                        v.w = pack_bf16(__uint_as_float(r[8 * u + 6]) * gmul, __uint_as_float(r[8 * u + 7]) * gmul);
-                        d4[u] = v;
+                    for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]) * gmul;
+                    if (acc) {
+                        float4* a4 = reinterpret_cast<float4*>(acc + c * 32);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            float4 x = a4[u];
+                            x.x += f[4 * u]; x.y += f[4 * u + 1]; x.z += f[4 * u + 2]; x.w += f[4 * u + 3];
+                            a4[u] = x;
+                            f[4 * u] = x.x; f[4 * u + 1] = x.y; f[4 * u + 2] = x.z; f[4 * u + 3] = x.w;
+                        }
+                    }
+                    if (emit) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint4 v;
+                            v.x = pack_bf16(f[8 * u + 0], f[8 * u + 1]);
+                            v.y = pack_bf16(f[8 * u + 2], f[8 * u + 3]);
+                            v.z = pack_bf16(f[8 * u + 4], f[8 * u + 5]);
+                            v.w = pack_bf16(f[8 * u + 6], f[8 * u + 7]);
+                            d4[u] = v;
+                        }
                     }
                 }
             }
@@ -402,9 +428,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             int32_t it, bh;
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const BwdItem item = a.items[it];
-            const int nq = (item.q_end - item.j0 + 127) / 128;
+            const int nq = (item.q_end - item.q_lo + 127) / 128;
             for (int i = 0; i < nq; ++i, ++gb) {
-                const int i0 = item.j0 + (nq - 1 - i) * 128;
+                const int i0 = item.q_lo + (nq - 1 - i) * 128;
                 const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
                 uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
@@ -439,7 +465,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 if (qrow == 0) {
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0, bh);
+                    for (int cc = 0; cc < D / 32; ++cc)
+                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 - a.row0, bh);
                     bulk_commit();
                     bulk_wait_read_all();
                     mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage
@@ -472,7 +499,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq;
     TcMaps mp{1, 2, 3};
     if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, a.g, mp) || !make_tile_map(&mv, a.v, a.g, mp) ||
-        !make_tile_map(&mdo, a.dout, a.g, mp) || !make_dq_acc_map(&mdq, a.dq_acc, a.g))
+        !make_tile_map(&mdo, a.dout, a.g, mp) || !make_dq_acc_map(&mdq, a.dq_acc, a.g, a.rows))
         return cudaErrorInvalidValue;
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
     if (work <= 0) return cudaSuccess;

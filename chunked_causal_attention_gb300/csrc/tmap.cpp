@@ -58,11 +58,11 @@ bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) 
     return r == CUDA_SUCCESS;
 }
 
-bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g) {
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows) {
     auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.T, (cuuint64_t)g.B * (cuuint64_t)g.H};
-    cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)g.T * g.D * 4};
+    if (!enc || rows <= 0) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)rows, (cuuint64_t)g.B * (cuuint64_t)g.H};
+    cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)rows * g.D * 4};
     cuuint32_t box[3] = {32, 128, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, es,

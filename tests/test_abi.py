@@ -147,3 +147,33 @@ def test_compute_calls_reject_bad_arguments_on_host():
     assert L.attn_fwd(fake, fake, fake, bad, nb, ctypes.byref(s), fake, fake, ws, 1 << 30, None) == 1
     assert L.attn_status(None, None) == 1
     assert cca.strerror(4).startswith("workspace")
+
+
+def test_chunk_backward_workspace_and_host_errors():
+    """attn_bwd_chunk (pass 2): one chunk, delta and the dQ accumulator sized
+    for the chunk's rows; argument errors found before any CUDA call."""
+    s = shape()                                                 # B1 H2 T1024 D64
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_workspace_size(s, cca.attn_plan(1024, 4, 0), 2)   # not one chunk
+    assert e.value.status == 1
+    n1 = cca.attn_workspace_size(s, [(256, 512, 0, 0)], 2)
+    n2 = cca.attn_workspace_size(s, [(256, 1024, 0, 0)], 2)
+    assert n1 >= 2 * 256 * (64 + 1) * 4 and n2 - n1 >= 2 * 512 * (64 + 1) * 4 - 1024
+    with pytest.raises(cca.AttnError):
+        cca.attn_workspace_size(s, [(512, 256, 0, 0)], 2)
+    L = cca.lib()
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    one, _ = _lib.chunk_array([(256, 512, 0, 0)])
+    args = [fake] * 6
+
+    def call(chunk=one, dk_acc=fake, dv_acc=fake, ws_bytes=1 << 30):
+        return L.attn_bwd_chunk(*args, chunk, ctypes.byref(s), fake, fake, fake, dk_acc, dv_acc, ws, ws_bytes,
+                                None)
+    assert call(dk_acc=None) == 1
+    assert call(dv_acc=ctypes.c_void_p(4100)) == 2
+    assert call(ws_bytes=n1 - 1) == 4
+    bad, _ = _lib.chunk_array([(256, 2000, 0, 0)])
+    assert call(chunk=bad) == 1
+    nested, _ = _lib.chunk_array([(256, 512, 300, 0)])            # ctx_begin after q_begin
+    assert call(chunk=nested) == 1
