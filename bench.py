@@ -292,7 +292,7 @@ def run_ours(args):
     # resident keys before it), the backward one chunk at a time in reverse
     # order (attn_bwd_chunk) with fp32 dK/dV accumulators that the calls share.
     ws_fc = cca.workspace(shape, chunks, cca.PASS_FWD, dev, per_chunk=True)
-    ws_bc = cca.workspace(shape, chunks, cca.PASS_BWD_CHUNK, dev)
+    ws_bc = cca.workspace(shape, chunks, cca.PASS_BWD_CHUNK, dev, per_chunk=True)
     dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=dev)
     dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=dev)
 
@@ -306,7 +306,7 @@ def run_ours(args):
         dk_acc.zero_()
         dv_acc.zero_()
         for c in reversed(chunks):
-            cca.attn_bwd_chunk(q, k, v, o, lse, do, c, shape, dq, dk, dv, dk_acc, dv_acc, ws_bc, stream)
+            cca.attn_bwd_chunk(q, k, v, o, lse, do, [c], shape, dq, dk, dv, dk_acc, dv_acc, ws_bc, stream)
         if ev is not None:
             ev[2].record(stream)
 

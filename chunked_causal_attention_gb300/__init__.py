@@ -24,12 +24,13 @@ __all__ = ["AttnError", "EXPORTS", "PLAN_UNIFORM", "PLAN_FLOPS", "PLAN_FLOPS_RES
 
 def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", per_chunk: bool = False):
     """A uint8 device buffer of the size the library asks for (pass 0 forward,
-    1 backward, 2 backward of one chunk), with its 256-byte status header
-    zeroed. per_chunk (always for pass 2): large enough for a call on any one
-    of the chunks alone."""
+    1 backward, 2 chunk-streamed backward), with its 256-byte status header
+    zeroed. per_chunk: ``chunks`` is a list of calls (each a chunk or a list
+    of chunks) and the buffer fits any one of them."""
     import torch
-    if per_chunk or pass_ == PASS_BWD_CHUNK:
-        n = max(attn_workspace_size(shape, [c], pass_) for c in chunks)
+    if per_chunk:
+        calls = [c if isinstance(c[0], (list, tuple)) else [c] for c in chunks]
+        n = max(attn_workspace_size(shape, c, pass_) for c in calls)
     else:
         n = attn_workspace_size(shape, chunks, pass_)
     ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
@@ -62,30 +63,34 @@ def backward(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = N
 
 
 def forward_streamed(q, k, v, chunks: Sequence, scale: Optional[float] = None, packed: bool = False, stream=None):
-    """The forward one chunk at a time, in chunk order: each call computes one
-    chunk's rows against the keys before it, which are resident in k, v."""
+    """The forward one call at a time, in order: each entry of ``chunks`` is a
+    chunk or a list of chunks (one call, e.g. an InfiniPipe batched or hybrid
+    chunk); each call computes its rows against the keys before them, which
+    are resident in k, v."""
     import torch
     shape = shape_of(q, scale, packed)
     o = torch.empty_like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
-    ws = workspace(shape, chunks, PASS_FWD, q.device, per_chunk=True)
-    for c in chunks:
-        attn_fwd(q, k, v, [c], shape, o, lse, ws, stream)
+    calls = [c if isinstance(c[0], (list, tuple)) else [c] for c in chunks]
+    ws = workspace(shape, calls, PASS_FWD, q.device, per_chunk=True)
+    for c in calls:
+        attn_fwd(q, k, v, c, shape, o, lse, ws, stream)
     return o, lse
 
 
 def backward_streamed(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = None, packed: bool = False,
                       stream=None):
-    """The backward one chunk at a time, in reverse chunk order, with fp32
-    dK/dV accumulators shared by the calls (attn_bwd_chunk). Returns
-    (dq, dk, dv, dk_acc, dv_acc)."""
+    """The backward one call at a time, in reverse order (entries of
+    ``chunks`` as forward_streamed), with fp32 dK/dV accumulators shared by
+    the calls (attn_bwd_chunk). Returns (dq, dk, dv, dk_acc, dv_acc)."""
     import torch
     shape = shape_of(q, scale, packed)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     # fp32 accumulators at the same element offsets as k and v
     dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=k.device).zero_()
     dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=v.device).zero_()
-    ws = workspace(shape, chunks, PASS_BWD_CHUNK, q.device)
-    for c in reversed(list(chunks)):
+    calls = [c if isinstance(c[0], (list, tuple)) else [c] for c in chunks]
+    ws = workspace(shape, calls, PASS_BWD_CHUNK, q.device, per_chunk=True)
+    for c in reversed(calls):
         attn_bwd_chunk(q, k, v, o, lse, dout, c, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream)
     return dq, dk, dv, dk_acc, dv_acc

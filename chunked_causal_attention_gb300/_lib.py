@@ -74,8 +74,8 @@ _SIG = {
     "attn_bwd_tiles": ([_VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
                        ctypes.c_int),
     "attn_bwd_dq": ([_CP, _I32, _SP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
-    "attn_bwd_chunk": ([_VP, _VP, _VP, _VP, _VP, _VP, _CP, _SP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
-                       ctypes.c_int),
+    "attn_bwd_chunk": ([_VP, _VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
+                        _VP], ctypes.c_int),
     "attn_fwd_noalloc": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP], ctypes.c_int),
     "attn_status": ([_VP, _VP], ctypes.c_int),
     "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -225,10 +225,10 @@ def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
                                             ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def attn_bwd_chunk(q, k, v, o, lse, dout, chunk, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream=None) -> None:
-    """Backward of one chunk's rows (chunk-streamed; see include/attn.h)."""
-    arr, n = chunk_array([chunk])
-    _check("attn_bwd_chunk", lib().attn_bwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr,
+def attn_bwd_chunk(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream=None) -> None:
+    """Backward of the rows of a set of chunks (chunk-streamed; see include/attn.h)."""
+    arr, n = chunk_array(chunks)
+    _check("attn_bwd_chunk", lib().attn_bwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr, n,
                                                   ctypes.byref(shape), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk_acc),
                                                   _ptr(dv_acc), _ptr(ws), ws.numel() * ws.element_size(),
                                                   _stream(stream)))

@@ -118,8 +118,9 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
 // --------------------------------------------------------------- backward layout
 struct BwdLayout {
     std::vector<BwdItem> items;
-    int32_t row0, rows;   // token rows held by delta and the dQ accumulator
-    size_t off_items, off_delta, off_dq, bytes;
+    std::vector<RowSeg> segs;   // workspace rows <-> tokens
+    int32_t rows;               // workspace rows of delta and the dQ accumulator per (batch, head)
+    size_t off_items, off_segs, off_delta, off_dq, bytes;
 };
 
 void bwd_finish_layout(const Geom& g, BwdLayout& L) {
@@ -129,7 +130,8 @@ void bwd_finish_layout(const Geom& g, BwdLayout& L) {
         return (a.q_end - a.q_lo) > (b.q_end - b.q_lo);
     });
     L.off_items = kHeaderBytes;
-    L.off_delta = L.off_items + round_up(L.items.size() * sizeof(BwdItem), kAlign);
+    L.off_segs = L.off_items + round_up(L.items.size() * sizeof(BwdItem), kAlign);
+    L.off_delta = L.off_segs + round_up(L.segs.size() * sizeof(RowSeg), kAlign);
     L.off_dq = L.off_delta + round_up((size_t)BH * L.rows * sizeof(float), kAlign);
     L.bytes = L.off_dq + round_up((size_t)BH * L.rows * g.D * sizeof(float), kAlign);
 }
@@ -144,24 +146,43 @@ void bwd_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
         int32_t j = i + 1;
         while (j < n && c[j].ctx_begin == s) { e = c[j].q_end; ++j; }
         for (int32_t j0 = s; j0 < e; j0 += kTile)
-            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, e), e, j0});
+            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, e), e, j0, 0, 0, {0, 0}});
         i = j;
     }
-    L.row0 = 0;
+    L.segs.assign(1, RowSeg{0, 0, g.T});
     L.rows = g.T;
     bwd_finish_layout(g, L);
 }
 
-// Backward of one chunk: one item per key tile of the chunk's context
+// Backward of a set of chunks: one item per key tile of each chunk's context
 // [ctx_begin, q_end); a tile's queries are the chunk's rows at or after its
-// first key. delta and dQ cover the chunk's rows only.
-void bwd_chunk_layout(const Geom& g, const attn_chunk& c, BwdLayout& L) {
+// first key. delta and dQ hold the chunks' rows, one segment after another.
+void bwd_chunk_layout(const Geom& g, const attn_chunk* c, int32_t n, BwdLayout& L) {
     L.items.clear();
-    for (int32_t j0 = c.ctx_begin; j0 < c.q_end; j0 += kTile)
-        L.items.push_back(BwdItem{j0, std::min(j0 + kTile, c.q_end), c.q_end, std::max(j0, c.q_begin)});
-    L.row0 = c.q_begin;
-    L.rows = c.q_end - c.q_begin;
+    L.segs.clear();
+    int32_t base = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const attn_chunk& x = c[i];
+        const int32_t off = base - x.q_begin;
+        for (int32_t j0 = x.ctx_begin; j0 < x.q_end; j0 += kTile)
+            L.items.push_back(BwdItem{j0, std::min(j0 + kTile, x.q_end), x.q_end, std::max(j0, x.q_begin), off,
+                                      x.q_begin, {0, 0}});
+        L.segs.push_back(RowSeg{base, x.q_begin, x.q_end - x.q_begin});
+        base += x.q_end - x.q_begin;
+    }
+    L.rows = base;
     bwd_finish_layout(g, L);
+}
+
+// Chunk-streamed backward: forward rules, plus disjoint key ranges: no chunk's
+// context reaches into an earlier chunk of the same call.
+int check_chunks_stream(const attn_chunk* c, int32_t n, int32_t T) {
+    int st = check_chunks_fwd(c, n, T);
+    if (st) return st;
+    if (n <= 0) return ATTN_E_INVAL;
+    for (int32_t i = 1; i < n; ++i)
+        if (c[i].ctx_begin < c[i - 1].q_end) return ATTN_E_INVAL;
+    return ATTN_OK;
 }
 
 }  // namespace
@@ -250,17 +271,22 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
 enum BwdStage { kPrep = 1, kTiles = 2, kDq = 4 };
 
 // Enqueue the stages of a backward laid out in L. dk_acc/dv_acc non-null:
-// chunk-streamed epilogue (fp32 accumulation, bf16 from key emit_from on).
+// chunk-streamed epilogue (fp32 accumulation, bf16 from each item's emit_from on).
 int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, const void* v, const void* o,
                const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dk_acc, float* dv_acc,
-               int32_t emit_from, void* ws, cudaStream_t s, int stages) {
+               void* ws, cudaStream_t s, int stages) {
     int st;
     uint8_t* w = (uint8_t*)ws;
     float* delta = (float*)(w + L.off_delta);
     float* dq_acc = (float*)(w + L.off_dq);
+    const RowSeg* segs = (const RowSeg*)(w + L.off_segs);
+    const int32_t n_segs = (int32_t)L.segs.size();
+    if (stages & (kPrep | kDq)) {
+        if ((st = upload(w + L.off_segs, L.segs.data(), L.segs.size() * sizeof(RowSeg), s))) return st;
+    }
     if (stages & kPrep) {
         if ((st = reset_header(ws, s))) return st;
-        PrepArgs a{o, dout, delta, dq_acc, L.row0, L.rows, g};
+        PrepArgs a{o, dout, delta, dq_acc, segs, n_segs, L.rows, g};
         if ((st = launched(launch_bwd_prep(a, s)))) return st;
     }
     if (stages & kTiles) {
@@ -268,8 +294,8 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
         BwdArgs a;
         a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
         a.dk = dk; a.dv = dv; a.dq_acc = dq_acc;
-        a.row0 = L.row0; a.rows = L.rows;
-        a.dk_acc = dk_acc; a.dv_acc = dv_acc; a.emit_from = emit_from;
+        a.rows = L.rows;
+        a.dk_acc = dk_acc; a.dv_acc = dv_acc;
         a.status = (uint32_t*)ws;
         a.items = (const BwdItem*)(w + L.off_items);
         a.n_items = (int32_t)L.items.size();
@@ -279,7 +305,7 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
         if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
     }
     if (stages & kDq) {
-        DqArgs a{dq_acc, dq, L.row0, L.rows, g};
+        DqArgs a{dq_acc, dq, segs, n_segs, L.rows, g};
         if ((st = launched(launch_bwd_dq(a, s)))) return st;
     }
     return ATTN_OK;
@@ -301,7 +327,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
     BwdLayout L;
     bwd_layout(g, chunks, n, L);
     if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
-    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, nullptr, nullptr, 0, ws, s, stages);
+    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, nullptr, nullptr, ws, s, stages);
 }
 
 }  // namespace
@@ -325,10 +351,9 @@ int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32
         bwd_layout(g, chunks, n, L);
         *bytes = L.bytes;
     } else if (pass == 2) {
-        if (n != 1) return ATTN_E_INVAL;
-        if ((st = check_chunks_fwd(chunks, n, g.T))) return st;
+        if ((st = check_chunks_stream(chunks, n, g.T))) return st;
         BwdLayout L;
-        bwd_chunk_layout(g, chunks[0], L);
+        bwd_chunk_layout(g, chunks, n, L);
         *bytes = L.bytes;
     } else {
         return ATTN_E_INVAL;
@@ -380,22 +405,22 @@ int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape, vo
 }
 
 int attn_bwd_chunk(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dout, const attn_chunk* chunk, const attn_shape* shape, void* dq, void* dk,
-                   void* dv, float* dk_acc, float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
+                   const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape, void* dq,
+                   void* dk, void* dv, float* dk_acc, float* dv_acc, void* ws, size_t ws_bytes, void* stream) {
     Geom g;
     int st = check_shape(shape, &g);
     if (st) return st;
-    if ((st = check_chunks_fwd(chunk, 1, g.T))) return st;
+    if ((st = check_chunks_stream(chunks, n, g.T))) return st;
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc};
     for (const void* p : ptrs)
         if (!p) return ATTN_E_INVAL;
     for (const void* p : ptrs)
         if (!aligned16(p)) return ATTN_E_ALIGN;
     BwdLayout L;
-    bwd_chunk_layout(g, *chunk, L);
+    bwd_chunk_layout(g, chunks, n, L);
     if ((st = check_ws(ws, ws_bytes, L.bytes))) return st;
-    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc, chunk->q_begin, ws,
-                      (cudaStream_t)stream, kPrep | kTiles | kDq);
+    return bwd_launch(g, L, q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc, ws, (cudaStream_t)stream,
+                      kPrep | kTiles | kDq);
 }
 
 int attn_status(void* ws, void* stream) {

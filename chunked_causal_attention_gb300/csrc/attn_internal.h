@@ -44,13 +44,24 @@ static_assert(sizeof(MergeSeg) == 32, "MergeSeg layout");
 // One backward work item: keys [j0, j1) (j1 - j0 <= 128) of a document;
 // the queries [q_lo, q_end) are walked in blocks of 128 rows starting at
 // q_lo. Whole backward: q_lo = j0 and q_end = the document end. Backward of
-// one chunk [q_begin, q_end): q_lo = max(j0, q_begin).
+// a chunk [q_begin, q_end): q_lo = max(j0, q_begin). Token t's row in delta
+// and in the dQ accumulator is t + row_off. Chunk-streamed epilogue: keys >=
+// emit_from (the chunk's q_begin) are written as bf16.
 struct BwdItem {
     int32_t j0, j1;
     int32_t q_end;
     int32_t q_lo;
+    int32_t row_off;
+    int32_t emit_from;
+    int32_t pad[2];
 };
-static_assert(sizeof(BwdItem) == 16, "BwdItem layout");
+static_assert(sizeof(BwdItem) == 32, "BwdItem layout");
+
+// Workspace rows [ws_row0, ws_row0 + R) of delta and the dQ accumulator hold
+// tokens [t0, t0 + R) (one segment per chunk; one for the whole backward).
+struct RowSeg {
+    int32_t ws_row0, t0, R;
+};
 
 struct Geom {
     int32_t B, H, T, D;
@@ -80,12 +91,13 @@ struct MergeArgs {
     Geom g;
 };
 
-// delta and the dQ accumulator hold rows [row0, row0 + rows) of every
-// (batch, head): delta[bh*rows + t - row0], dq_acc[(bh*rows + t - row0)*D + d].
+// delta and the dQ accumulator hold `rows` workspace rows per (batch, head):
+// delta[bh*rows + r], dq_acc[(bh*rows + r)*D + d]; segs map rows to tokens.
 struct PrepArgs {
     const void* o; const void* dout;
     float* delta; float* dq_acc;
-    int32_t row0, rows;
+    const RowSeg* segs; int32_t n_segs;
+    int32_t rows;
     Geom g;
 };
 
@@ -94,12 +106,11 @@ struct BwdArgs {
     const float* lse; const float* delta;
     void* dk; void* dv;
     float* dq_acc;
-    int32_t row0, rows;   // rows of delta and dq_acc (layout as PrepArgs)
+    int32_t rows;         // workspace rows of delta and dq_acc per (batch, head)
     // Chunk-streamed backward: fp32 dK/dV accumulators (element offsets of the
     // bf16 tensors); the epilogue adds into them and writes bf16 dk/dv only for
-    // keys >= emit_from. Null for the whole backward (bf16 written directly).
+    // keys >= the item's emit_from. Null for the whole backward (bf16 written).
     float* dk_acc; float* dv_acc;
-    int32_t emit_from;
     uint32_t* status;
     const BwdItem* items;
     int32_t n_items;
@@ -115,9 +126,10 @@ struct BwdArgs {
 void wait_settings(uint64_t* wait_ns, int32_t* stall);
 
 struct DqArgs {
-    const float* dq_acc;  // rows [row0, row0 + rows) as PrepArgs
+    const float* dq_acc;  // rows as PrepArgs
     void* dq;
-    int32_t row0, rows;
+    const RowSeg* segs; int32_t n_segs;
+    int32_t rows;
     Geom g;
 };
 

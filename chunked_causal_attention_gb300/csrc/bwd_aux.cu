@@ -2,13 +2,23 @@
 //   prep: D_t = sum_d dO_td * O_td in fp32 (the row term of dS = P o (dP - D)),
 //         and zeroing of the fp32 dQ accumulator.
 //   dq:   dQ = bf16(fp32 accumulator), written with the caller's strides.
-// One warp per (batch*head, token) of the rows [row0, row0 + rows) the
-// workspace holds (all tokens for the whole backward, one chunk's rows for
-// the chunk-streamed backward).
+// One warp per (batch*head, workspace row); the rows are the tokens of one or
+// more segments (all tokens for the whole backward, the chunks' rows for the
+// chunk-streamed backward).
 #include "device_common.cuh"
 
 namespace attn {
 namespace {
+
+// Token of workspace row r: the segment with the largest ws_row0 <= r.
+__device__ __forceinline__ int token_of_row(const RowSeg* segs, int n, int r) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (segs[mid].ws_row0 <= r) lo = mid; else hi = mid - 1;
+    }
+    return segs[lo].t0 + (r - segs[lo].ws_row0);
+}
 
 // One warp per (batch*head, token): delta = dO . O; zero the dQ accumulator row.
 template <int D>
@@ -18,7 +28,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
-    const int bh = (int)(w / a.rows), t = a.row0 + (int)(w % a.rows);
+    const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
     const int b = bh / a.g.H, h = bh % a.g.H;
     const int64_t off = (int64_t)b * a.g.sb + (int64_t)h * a.g.sh + (int64_t)t * a.g.st + lane * PER;
     const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o) + off;
@@ -48,7 +58,7 @@ __global__ void __launch_bounds__(256) dq_kernel(DqArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
-    const int bh = (int)(w / a.rows), t = a.row0 + (int)(w % a.rows);
+    const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
     const int b = bh / a.g.H, h = bh % a.g.H;
     const float* src = a.dq_acc + w * D + lane * PER;
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +

@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const BwdItem item = a.items[it];
             const int nq = (item.q_end - item.q_lo + 127) / 128;
             const int key = item.j0 + krow;
-            // src[t] for a token t: LSE (all tokens) or delta (rows [row0, row0 + rows))
-            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.rows - a.row0;
+            // src[t] for a token t: LSE (all tokens) or delta (workspace row t + row_off)
+            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.rows + item.row_off;
             const float mul = stage_l ? -kLog2e : -1.f;
             // raw value of the next block, scaled only when it is staged, so the
             // load's latency is not waited for until then
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             // chunk-streamed backward: add into the fp32 accumulator row, and write
             // bf16 only for the chunk's own keys (complete once their chunk has run)
             float* acc = a.dk_acc ? (grp == 0 ? a.dk_acc : a.dv_acc) + roff : nullptr;
-            const bool emit = acc == nullptr || key >= a.emit_from;
+            const bool emit = acc == nullptr || key >= item.emit_from;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc)
-                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 - a.row0, bh);
+                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 + item.row_off, bh);
                     bulk_commit();
                     bulk_wait_read_all();
                     mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage

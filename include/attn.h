@@ -110,8 +110,8 @@ int attn_plan_varlen(const int64_t* cu_seqlens, int32_t ndocs, int32_t max_chunk
                      int32_t mode, attn_chunk* out, int32_t cap, int32_t* n_out);
 
 /* Workspace bytes for pass 0 (forward: attn_fwd and its stages), pass 1
- * (backward: attn_bwd and its stages) or pass 2 (attn_bwd_chunk; n must be 1
- * and chunks the one chunk) of this shape and chunk table.
+ * (backward: attn_bwd and its stages) or pass 2 (attn_bwd_chunk on exactly
+ * these chunks) of this shape and chunk table.
  * Validates like the compute calls. */
 int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32_t n,
                         int32_t pass, size_t* bytes);
@@ -173,34 +173,38 @@ int attn_bwd_dq(const attn_chunk* chunks, int32_t n, const attn_shape* shape,
 
 /* ---- chunk-streamed backward ------------------------------------------- */
 
-/* Backward of ONE chunk's query rows against its resident context, for a
- * caller that runs the chunks of a document one at a time: the forward in
- * chunk order (attn_fwd with the single chunk: its rows attend to the keys
+/* Backward of the query rows of a set of chunks against their resident
+ * contexts, for a caller that runs chunks one call at a time: the forward in
+ * chunk order (attn_fwd on the same chunks: their rows attend to the keys
  * [ctx_begin, q_end) already in k, v; SPPO §5.1, the K/V of earlier
- * subsequences stay resident), the backward in reverse chunk order
- * (InfiniPipe §II-A: the K/V gradients of a token gather contributions from
- * every later token, so a chunk's keys are complete once the chunks after it
- * and the chunk itself have run).
- * For the query rows t in [q_begin, q_end) of *chunk (kv_split is ignored):
+ * subsequences stay resident), the backward in reverse order (InfiniPipe
+ * §II-A: the K/V gradients of a token gather contributions from every later
+ * token, so a chunk's keys are complete once the chunks after it and the
+ * chunk itself have run). One call may hold the slices of several documents,
+ * such as an InfiniPipe batched or hybrid chunk {C, S} (§III-A1).
+ * For each chunk, with query rows t in [q_begin, q_end) (kv_split ignored):
  *   dq rows [q_begin, q_end)                 = their gradient (bf16; complete:
  *                                              every key they see is in the
  *                                              context);
  *   dk_acc, dv_acc rows [ctx_begin, q_end)  += the rows' contributions (fp32,
  *                                              dK including the scale);
  *   dk, dv rows [q_begin, q_end)             = bf16 of the updated accumulators.
- * Other rows of dq, dk, dv, dk_acc, dv_acc are not touched. Zero dk_acc and
- * dv_acc over a document before its last chunk's call; after the calls for
- * all of its chunks in reverse order, dq, dk, dv equal attn_bwd's result for
- * the document. o, lse are the forward's; o and dout are read for the
- * chunk's rows. dk_acc, dv_acc: fp32 device arrays indexed like the bf16
- * tensors, element (b, t, h, d) at b*sb + t*st + h*sh + d, 16-byte aligned.
- * The workspace comes from attn_workspace_size(pass 2) for this chunk; calls
- * that share dk_acc/dv_acc rows must run one after another (one stream).
- * Errors: ATTN_E_INVAL (bad shape or chunk, a NULL pointer), ATTN_E_ALIGN,
- * ATTN_E_UNSUPPORTED, ATTN_E_WORKSPACE, ATTN_E_CUDA; device errors through
- * attn_status(ws). */
+ * Other rows of dq, dk, dv, dk_acc, dv_acc are not touched. Chunks: sorted by
+ * q_begin, 0 <= ctx_begin <= q_begin < q_end <= T, and key ranges disjoint
+ * (each ctx_begin >= the previous chunk's q_end), so that no accumulator row
+ * is updated twice by one call. Zero dk_acc and dv_acc over a document before
+ * the call holding its last chunk; after the calls holding all of its chunks,
+ * in reverse chunk order, dq, dk, dv equal attn_bwd's result for the document.
+ * o, lse are the forward's; o and dout are read for the chunks' rows.
+ * dk_acc, dv_acc: fp32 device arrays indexed like the bf16 tensors, element
+ * (b, t, h, d) at b*sb + t*st + h*sh + d, 16-byte aligned. The workspace comes
+ * from attn_workspace_size(pass 2) for the same chunks; calls that share
+ * dk_acc/dv_acc rows must run one after another (one stream).
+ * Errors: ATTN_E_INVAL (bad shape or chunks, overlapping key ranges, a NULL
+ * pointer), ATTN_E_ALIGN, ATTN_E_UNSUPPORTED, ATTN_E_WORKSPACE, ATTN_E_CUDA;
+ * device errors through attn_status(ws). */
 int attn_bwd_chunk(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dout, const attn_chunk* chunk, const attn_shape* shape,
+                   const void* dout, const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                    void* dq, void* dk, void* dv, float* dk_acc, float* dv_acc,
                    void* ws, size_t ws_bytes, void* stream);
 

@@ -150,12 +150,15 @@ def test_compute_calls_reject_bad_arguments_on_host():
 
 
 def test_chunk_backward_workspace_and_host_errors():
-    """attn_bwd_chunk (pass 2): one chunk, delta and the dQ accumulator sized
-    for the chunk's rows; argument errors found before any CUDA call."""
+    """attn_bwd_chunk (pass 2): delta and the dQ accumulator sized for the
+    chunks' rows; chunks of one call must have disjoint key ranges; argument
+    errors found before any CUDA call."""
     s = shape()                                                 # B1 H2 T1024 D64
     with pytest.raises(cca.AttnError) as e:
-        cca.attn_workspace_size(s, cca.attn_plan(1024, 4, 0), 2)   # not one chunk
+        cca.attn_workspace_size(s, cca.attn_plan(1024, 4, 0), 2)   # later chunks' contexts overlap earlier ones
     assert e.value.status == 1
+    two = cca.attn_workspace_size(s, [(0, 100, 0, 0), (300, 400, 100, 0)], 2)   # two documents
+    assert two >= 2 * 200 * (64 + 1) * 4
     n1 = cca.attn_workspace_size(s, [(256, 512, 0, 0)], 2)
     n2 = cca.attn_workspace_size(s, [(256, 1024, 0, 0)], 2)
     assert n1 >= 2 * 256 * (64 + 1) * 4 and n2 - n1 >= 2 * 512 * (64 + 1) * 4 - 1024
@@ -167,8 +170,8 @@ def test_chunk_backward_workspace_and_host_errors():
     one, _ = _lib.chunk_array([(256, 512, 0, 0)])
     args = [fake] * 6
 
-    def call(chunk=one, dk_acc=fake, dv_acc=fake, ws_bytes=1 << 30):
-        return L.attn_bwd_chunk(*args, chunk, ctypes.byref(s), fake, fake, fake, dk_acc, dv_acc, ws, ws_bytes,
+    def call(chunk=one, dk_acc=fake, dv_acc=fake, ws_bytes=1 << 30, n=1):
+        return L.attn_bwd_chunk(*args, chunk, n, ctypes.byref(s), fake, fake, fake, dk_acc, dv_acc, ws, ws_bytes,
                                 None)
     assert call(dk_acc=None) == 1
     assert call(dv_acc=ctypes.c_void_p(4100)) == 2
@@ -177,3 +180,6 @@ def test_chunk_backward_workspace_and_host_errors():
     assert call(chunk=bad) == 1
     nested, _ = _lib.chunk_array([(256, 512, 300, 0)])            # ctx_begin after q_begin
     assert call(chunk=nested) == 1
+    overlap, _ = _lib.chunk_array([(0, 100, 0, 0), (100, 200, 0, 0)])   # second context covers the first chunk
+    assert call(chunk=overlap, n=2) == 1
+    assert call(n=0) == 1

@@ -102,7 +102,7 @@ def test_one_call_against_oracle_contributions():
     dk_acc[:, :, cb:qe] = 0
     dv_acc[:, :, cb:qe] = 0
     ws = cca.workspace(shape, [(qb, qe, cb, 0)], cca.PASS_BWD_CHUNK)
-    cca.attn_bwd_chunk(q, k, v, o, lse, do, (qb, qe, cb, 0), shape, dq, dk, dv, dk_acc, dv_acc, ws)
+    cca.attn_bwd_chunk(q, k, v, o, lse, do, [(qb, qe, cb, 0)], shape, dq, dk, dv, dk_acc, dv_acc, ws)
     torch.cuda.synchronize()
     assert cca.attn_status(ws) == 0
     sc = default_scale(D)
@@ -131,3 +131,32 @@ def test_streamed_7b_128k_sampled():
     sampled_rows_check(w, q, k, v, do, o, lse, dq, 2048, 11, "streamed 128k")
     tail_keys_check(w, q, k, v, do, dk, dv, [5], 32, 12, "streamed 128k")
     invariants_check(w, q, do, dk, dv, "streamed 128k")
+
+
+def test_calls_holding_several_documents():
+    """Calls that hold slices of several documents (InfiniPipe batched and
+    hybrid chunks {C, S}): a long document split into three slices, whose
+    tail shares a call with two short documents; another call batches three
+    short documents. Forward in call order, backward in reverse."""
+    lens = [1500, 200, 77, 300, 129, 1]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    L = cu[-1]
+    long0 = [(0, 700, 0, 0), (700, 1150, 0, 0)]                      # split chunks of document 0
+    hybrid = [(1150, 1500, 0, 0), (1500, 1700, 1500, 0), (1700, 1777, 1700, 0)]   # tail + two short docs
+    batched = [(1777, 2077, 1777, 0), (2077, 2206, 2077, 0), (2206, 2207, 2206, 0)]
+    calls = [[long0[0]], batched, [long0[1]], hybrid]
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, L, 128, seed=304, packed=True))
+    o, lse = cca.forward_streamed(q, k, v, calls, packed=True)
+    dq, dk, dv, dk_acc, dv_acc = cca.backward_streamed(q, k, v, o, lse, do, calls, packed=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, dk_acc.to(torch.bfloat16)) and torch.equal(dv, dv_acc.to(torch.bfloat16))
+    sc = default_scale(128)
+    for h in range(2):
+        qh, kh, vh, doh = (head(x, 0, h, True) for x in (q, k, v, do))
+        rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, sc, cu)
+        check_fwd(head(o, 0, h, True), lse_head(lse, 0, h), ro, rl, f"calls h{h}")
+        check_grad(head(dq, 0, h, True), rdq, f"calls dQ h{h}")
+        check_grad(head(dk, 0, h, True), rdk, f"calls dK h{h}")
+        check_grad(head(dv, 0, h, True), rdv, f"calls dV h{h}")
