@@ -24,7 +24,7 @@ PLAN_FLOPS = 1
 PLAN_FLOPS_RESPLIT_EDGES = 2
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
+EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
            "attn_bwd_chunk", "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
 
@@ -64,6 +64,9 @@ _SP = ctypes.POINTER(attn_shape)
 _SIG = {
     "attn_plan": ([_I64, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
     "attn_plan_varlen": ([ctypes.POINTER(_I64), _I32, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "attn_plan_infinipipe": ([ctypes.POINTER(_I64), _I32, _I32, _I64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                              _CP, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _I32, ctypes.POINTER(_I32)],
+                             ctypes.c_int),
     "attn_workspace_size": ([_SP, _CP, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "attn_fwd": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
     "attn_fwd_tiles": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, ctypes.c_size_t, _VP], ctypes.c_int),
@@ -141,6 +144,26 @@ def attn_plan_varlen(cu_seqlens: Sequence[int], max_chunk_tokens: int, mode: int
             continue
         _check("attn_plan_varlen", st)
         return [(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[:n.value]]
+
+
+def attn_plan_infinipipe(seq_lens: Sequence[int], K: int, token_cap: int, alpha1: float, alpha2: float,
+                         beta1: float) -> List[List[Tuple[int, int, int, int]]]:
+    """InfiniPipe Algorithm 1: a list of calls, each a list of chunks in the
+    packed layout of ``seq_lens`` (see include/attn.h)."""
+    lens = (_I64 * max(1, len(seq_lens)))(*[int(x) for x in seq_lens])
+    n, nc = _I32(0), _I32(0)
+    cap, ccap = 16, 16
+    while True:
+        out = (attn_chunk * cap)()
+        off = (_I32 * ccap)()
+        st = lib().attn_plan_infinipipe(lens, len(seq_lens), K, token_cap, alpha1, alpha2, beta1, out, cap,
+                                        ctypes.byref(n), off, ccap, ctypes.byref(nc))
+        if st == 8:                          # ATTN_E_CAPACITY reports the needed counts
+            cap, ccap = max(cap, n.value), max(ccap, nc.value + 1)
+            continue
+        _check("attn_plan_infinipipe", st)
+        return [[(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[off[i]:off[i + 1]]]
+                for i in range(nc.value)]
 
 
 # ------------------------------------------------------------------ shapes

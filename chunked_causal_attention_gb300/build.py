@@ -33,7 +33,7 @@ def nvcc() -> str:
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj, "-std=c++17", "-O3", "-lineinfo",
-           "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *ARCH]
+           "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off", "-I", INCLUDE, "-I", CSRC, *ARCH]
     if src.endswith(".cu"):
         cmd += ["-Xptxas", "-v"] if verbose else []
         cmd += ["--expt-relaxed-constexpr"]

@@ -110,3 +110,198 @@ extern "C" int attn_plan_varlen(const int64_t* cu, int32_t ndocs, int32_t max_ch
     if (mode == ATTN_PLAN_FLOPS_RESPLIT_EDGES) apply_resplit(c);
     return emit(c, out, cap, n_out);
 }
+
+// ---------------------------------------------------------------------------
+// InfiniPipe Algorithm 1, "Workload-Balanced Sequence Chunking" (§III-B), on
+// one GPU. Chunk cost by Eq. (1) with N = d_p = 1 and no all-to-all term:
+// beta1 plus, per slice of s tokens after C context tokens,
+// alpha1((C+s)^2 - C^2) + alpha2 s. Steps:
+//   1. mesh: the longest sequence cut into K slices of equal cost, each
+//      boundary the multiple of 128 nearest to the equal-cost point (ties up);
+//   2. every sequence longer than the next mesh slice takes it (split chunks);
+//      the rest is its tail slice; sequences no longer than the first mesh
+//      slice are short;
+//   3. one bucket per tail slice; short sequences from the most expensive
+//      down, each into the first bucket (by increasing time per token) within
+//      the time threshold T_t and token threshold T_m; a new bucket when even
+//      the emptiest bucket has no room; T_t loosened to the least time among
+//      buckets with room (plus the sequence's time) when no bucket fits.
+// T_t starts at the costliest mesh slice; T_m is the caller's token capacity.
+// Costs are float64 with the integer parts formed first, in a fixed order.
+namespace {
+
+struct IpCost {
+    double a1, a2, b1;
+    double slice_time(int64_t C, int64_t s) const {
+        const int64_t quad = (C + s) * (C + s) - C * C;
+        return a1 * (double)quad + a2 * (double)s;
+    }
+    double prefix(int64_t b) const { return a1 * (double)(b * b) + a2 * (double)b; }
+};
+
+struct IpMember {
+    int32_t seq;
+    int64_t ctx, len;
+};
+
+struct IpBucket {
+    int32_t order;
+    std::vector<IpMember> members;
+    double tot_time;
+    int64_t tot_tokens;
+};
+
+// Boundaries b_0..b_K of the mesh; false if they are not strictly increasing.
+bool ip_mesh(int64_t Lmax, int32_t K, const IpCost& c, std::vector<int64_t>& b) {
+    const double total = c.prefix(Lmax);
+    b.assign(K + 1, 0);
+    for (int32_t k = 1; k < K; ++k) {
+        const double target = (double)k * total;
+        // largest m with K * cost(128 m - 64) <= k * cost(Lmax); the test is
+        // monotone in m, so a bisection finds what a scan from m = 0 would
+        int64_t lo = 0, hi = Lmax / 128 + 2;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) / 2;
+            if ((double)K * c.prefix(128 * mid - 64) <= target)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        b[k] = 128 * lo;
+    }
+    b[K] = Lmax;
+    for (int32_t i = 0; i < K; ++i)
+        if (!(b[i] < b[i + 1])) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" int attn_plan_infinipipe(const int64_t* seq_lens, int32_t nseq, int32_t K, int64_t token_cap,
+                                    double alpha1, double alpha2, double beta1, attn_chunk* out, int32_t cap,
+                                    int32_t* n_out, int32_t* call_off, int32_t call_cap, int32_t* n_calls) {
+    if (!seq_lens || !n_out || !n_calls || nseq <= 0 || K <= 0 || token_cap <= 0) return ATTN_E_INVAL;
+    if ((!out && cap > 0) || cap < 0 || (!call_off && call_cap > 0) || call_cap < 0) return ATTN_E_INVAL;
+    if (!std::isfinite(alpha1) || !std::isfinite(alpha2) || !std::isfinite(beta1) || alpha1 < 0 || alpha2 < 0 ||
+        beta1 < 0 || (alpha1 == 0 && alpha2 == 0))
+        return ATTN_E_INVAL;
+    std::vector<int64_t> start(nseq + 1, 0);
+    int64_t Lmax = 0;
+    for (int32_t i = 0; i < nseq; ++i) {
+        if (seq_lens[i] < 0) return ATTN_E_INVAL;
+        start[i + 1] = start[i] + seq_lens[i];
+        if (start[i + 1] > INT32_MAX) return ATTN_E_INVAL;
+        Lmax = std::max(Lmax, seq_lens[i]);
+    }
+    std::vector<std::vector<attn_chunk>> calls;
+    if (Lmax > 0) {
+        const IpCost c{alpha1, alpha2, beta1};
+        std::vector<int64_t> b;
+        if (!ip_mesh(Lmax, K, c, b)) return ATTN_E_INVAL;
+        std::vector<int64_t> mesh(K);
+        for (int32_t i = 0; i < K; ++i) mesh[i] = b[i + 1] - b[i];
+        if (token_cap < mesh[0]) return ATTN_E_INVAL;
+        double T_t = 0;
+        for (int32_t i = 0; i < K; ++i) T_t = std::max(T_t, beta1 + c.slice_time(b[i], mesh[i]));
+        const int64_t T_m = token_cap;
+
+        // sharding by the mesh
+        std::vector<std::vector<std::pair<int64_t, int64_t>>> slices(nseq);   // (ctx, len)
+        std::vector<IpBucket> B;
+        std::vector<int32_t> shorts;
+        for (int32_t i = 0; i < nseq; ++i) {
+            const int64_t L = seq_lens[i];
+            if (L == 0) continue;
+            int64_t rem = L, ctx = 0;
+            for (int32_t j = 0; j < K && rem > mesh[j]; ++j) {
+                slices[i].push_back({ctx, mesh[j]});
+                ctx += mesh[j];
+                rem -= mesh[j];
+            }
+            if (slices[i].empty()) {
+                shorts.push_back(i);
+            } else {
+                IpBucket bk{(int32_t)B.size(), {IpMember{i, ctx, rem}}, beta1 + c.slice_time(ctx, rem), rem};
+                B.push_back(bk);
+            }
+        }
+        // short sequences from the most expensive down (ties: input order)
+        std::stable_sort(shorts.begin(), shorts.end(), [&](int32_t x, int32_t y) {
+            return c.slice_time(0, seq_lens[x]) > c.slice_time(0, seq_lens[y]);
+        });
+        std::vector<int32_t> byMetric;
+        for (int32_t i : shorts) {
+            const int64_t s = seq_lens[i];
+            const double t = c.slice_time(0, s);
+            for (;;) {
+                int64_t min_tok = INT64_MAX;
+                for (const IpBucket& bk : B) min_tok = std::min(min_tok, bk.tot_tokens);
+                if (B.empty() || min_tok + s > T_m) {
+                    B.push_back(IpBucket{(int32_t)B.size(), {IpMember{i, 0, s}}, beta1 + t, s});
+                    break;
+                }
+                byMetric.resize(B.size());
+                for (size_t x = 0; x < B.size(); ++x) byMetric[x] = (int32_t)x;
+                std::sort(byMetric.begin(), byMetric.end(), [&](int32_t x, int32_t y) {
+                    const double mx = B[x].tot_time / (double)B[x].tot_tokens;
+                    const double my = B[y].tot_time / (double)B[y].tot_tokens;
+                    return mx < my || (mx == my && B[x].order < B[y].order);
+                });
+                bool placed = false;
+                for (int32_t x : byMetric) {
+                    IpBucket& bk = B[x];
+                    if (bk.tot_time + t <= T_t && bk.tot_tokens + s <= T_m) {
+                        bk.members.push_back(IpMember{i, 0, s});
+                        bk.tot_time = bk.tot_time + t;
+                        bk.tot_tokens = bk.tot_tokens + s;
+                        placed = true;
+                        break;
+                    }
+                }
+                if (placed) break;
+                double least = 0;
+                bool any = false;
+                for (const IpBucket& bk : B)
+                    if (bk.tot_tokens + s <= T_m && (!any || bk.tot_time < least)) {
+                        least = bk.tot_time;
+                        any = true;
+                    }
+                T_t = least + t;
+            }
+        }
+        // split chunks by slice index, then the buckets in creation order
+        size_t depth = 0;
+        for (int32_t i = 0; i < nseq; ++i) depth = std::max(depth, slices[i].size());
+        for (size_t j = 0; j < depth; ++j)
+            for (int32_t i = 0; i < nseq; ++i)
+                if (j < slices[i].size()) {
+                    const int64_t s0 = start[i] + slices[i][j].first;
+                    calls.push_back({attn_chunk{(int32_t)s0, (int32_t)(s0 + slices[i][j].second), (int32_t)start[i], 0}});
+                }
+        for (const IpBucket& bk : B) {
+            std::vector<attn_chunk> v;
+            for (const IpMember& m : bk.members) {
+                const int64_t s0 = start[m.seq] + m.ctx;
+                v.push_back(attn_chunk{(int32_t)s0, (int32_t)(s0 + m.len), (int32_t)start[m.seq], 0});
+            }
+            std::sort(v.begin(), v.end(), [](const attn_chunk& x, const attn_chunk& y) { return x.q_begin < y.q_begin; });
+            calls.push_back(v);
+        }
+    }
+    int64_t total = 0;
+    for (const auto& v : calls) total += (int64_t)v.size();
+    if (total > cap || (int64_t)calls.size() + 1 > call_cap) {
+        *n_out = (int32_t)total;
+        *n_calls = (int32_t)calls.size();
+        return ATTN_E_CAPACITY;
+    }
+    int32_t pos = 0;
+    call_off[0] = 0;
+    for (size_t x = 0; x < calls.size(); ++x) {
+        for (const attn_chunk& ch : calls[x]) out[pos++] = ch;
+        call_off[x + 1] = pos;
+    }
+    *n_out = pos;
+    *n_calls = (int32_t)calls.size();
+    return ATTN_OK;
+}

@@ -109,6 +109,39 @@ int attn_plan(int64_t L, int32_t N, int32_t mode,
 int attn_plan_varlen(const int64_t* cu_seqlens, int32_t ndocs, int32_t max_chunk_tokens,
                      int32_t mode, attn_chunk* out, int32_t cap, int32_t* n_out);
 
+/* InfiniPipe's workload-balanced sequence chunking (Algorithm 1, §III-B),
+ * on one GPU. Inputs: nseq sequence lengths (packed back to back in this
+ * order, so sequence i starts at seq_lens[0] + ... + seq_lens[i-1]); K, the
+ * number of slices of the longest sequence; token_cap, the most tokens one
+ * chunk may hold (T_m); the cost model of Eq. (1) with N = d_p = 1: a chunk
+ * {C, S} costs beta1 + alpha1((C+s0)^2 - C^2) + alpha2 s0 + the sum over its
+ * other slices of alpha1 s^2 + alpha2 s.
+ * Steps: the longest sequence is cut into K slices of equal cost (the mesh;
+ * boundaries at the multiple of 128 nearest to each equal-cost point, ties
+ * up); each sequence takes mesh slices in order while it is longer than the
+ * next one (split chunks, one call each) and keeps the rest as its tail
+ * slice; sequences no longer than the first mesh slice are short. Every tail
+ * seeds a bucket (a hybrid chunk); short sequences, most expensive first, go
+ * into the first bucket in order of increasing time per token whose time
+ * stays within T_t (initially the costliest mesh slice) and whose tokens stay
+ * within token_cap; a sequence that even the emptiest bucket cannot hold
+ * opens a new bucket (a batched chunk); when no bucket fits, T_t is raised to
+ * the least time among buckets with token room plus the sequence's time.
+ * Output: the chunks of every call (chunk {C, S}), call after call, in out
+ * (ctx_begin = the sequence start, kv_split = 0, sorted by q_begin within a
+ * call); call c holds out[call_off[c] .. call_off[c+1]); *n_out chunks and
+ * *n_calls calls. The order can be run one call at a time: forward with
+ * attn_fwd in call order, backward with attn_bwd_chunk in reverse order.
+ * Errors: ATTN_E_INVAL (no sequence, a negative length, more than INT32_MAX
+ * tokens, K <= 0, costs negative or not finite or alpha1 = alpha2 = 0, a
+ * mesh whose boundaries are not strictly increasing, token_cap below the
+ * first mesh slice), ATTN_E_CAPACITY (cap < *n_out or call_cap < *n_calls + 1;
+ * both counts are then set to what is needed). Host only. */
+int attn_plan_infinipipe(const int64_t* seq_lens, int32_t nseq, int32_t K, int64_t token_cap,
+                         double alpha1, double alpha2, double beta1,
+                         attn_chunk* out, int32_t cap, int32_t* n_out,
+                         int32_t* call_off, int32_t call_cap, int32_t* n_calls);
+
 /* Workspace bytes for pass 0 (forward: attn_fwd and its stages), pass 1
  * (backward: attn_bwd and its stages) or pass 2 (attn_bwd_chunk on exactly
  * these chunks) of this shape and chunk table.

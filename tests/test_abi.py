@@ -183,3 +183,68 @@ def test_chunk_backward_workspace_and_host_errors():
     overlap, _ = _lib.chunk_array([(0, 100, 0, 0), (100, 200, 0, 0)])   # second context covers the first chunk
     assert call(chunk=overlap, n=2) == 1
     assert call(n=0) == 1
+
+
+def test_plan_infinipipe_matches_oracle_exactly():
+    """attn_plan_infinipipe (C++) against oracle.infinipipe on random inputs:
+    the same calls, chunk for chunk, including float64 threshold decisions."""
+    from oracle import infinipipe as IP
+    rng = random.Random(11)
+    checked = 0
+    for it in range(600):
+        n = rng.randint(1, 40)
+        top = rng.choice([300, 5000, 40000, 300000])
+        lengths = [rng.choice([0, rng.randint(1, 128), rng.randint(1, top)]) for _ in range(n)]
+        K = rng.randint(1, 10)
+        a1 = rng.choice([1.0, 3.3e-10, 1e-9, 7.1e-11])
+        a2 = rng.choice([0.0, 2.2e-5, 1e-3, 31.0])
+        b1 = rng.choice([0.0, 1e-4, 2.5])
+        cap = rng.choice([1000, 20000, 70000, 400000])
+        try:
+            want, _ = IP.plan(lengths, K, cap, IP.Cost(a1, a2, b1))
+        except IP.PlanError:
+            with pytest.raises(cca.AttnError) as e:
+                cca.attn_plan_infinipipe(lengths, K, cap, a1, a2, b1)
+            assert e.value.status == 1
+            continue
+        got = cca.attn_plan_infinipipe(lengths, K, cap, a1, a2, b1)
+        assert got == [list(c) for c in want], (lengths, K, cap, a1, a2, b1)
+        checked += 1
+    assert checked > 300
+
+
+def test_plan_infinipipe_workload_lengths():
+    """The packed 256K workload's document lengths (one 128K document and 15
+    shorter ones) with the costs and K used by the streamed measurement."""
+    from oracle import infinipipe as IP
+    from chunked_causal_attention_gb300.workloads import WORKLOADS
+    cu = WORKLOADS["packed_256k"].cu_seqlens()
+    lengths = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    for K, cap in [(4, 65536), (8, 65536), (16, 131072)]:
+        got = cca.attn_plan_infinipipe(lengths, K, cap, 1.0, 2000.0, 0.0)
+        want, info = IP.plan(lengths, K, cap, IP.Cost(1.0, 2000.0, 0.0))
+        assert got == [list(c) for c in want]
+        assert sum(qe - qb for call in got for qb, qe, _, _ in call) == cu[-1]
+
+
+def test_plan_infinipipe_errors():
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_plan_infinipipe([1000], 16, 10 ** 6, 1.0, 0.0, 0.0)       # mesh collapses
+    assert e.value.status == 1
+    with pytest.raises(cca.AttnError):
+        cca.attn_plan_infinipipe([4096, 10], 2, 1000, 1.0, 0.0, 0.0)        # capacity below the first slice
+    with pytest.raises(cca.AttnError):
+        cca.attn_plan_infinipipe([4096], 2, 4096, 0.0, 0.0, 1.0)            # no per-token cost
+    with pytest.raises(cca.AttnError):
+        cca.attn_plan_infinipipe([4096], 2, 4096, float("nan"), 0.0, 1.0)
+    with pytest.raises(cca.AttnError):
+        cca.attn_plan_infinipipe([4096, -1], 2, 4096, 1.0, 0.0, 0.0)
+    assert cca.attn_plan_infinipipe([0, 0], 2, 100, 1.0, 0.0, 0.0) == []
+    L = cca.lib()
+    lens = (ctypes.c_int64 * 3)(5000, 300, 200)
+    out = (_lib.attn_chunk * 1)()
+    off = (ctypes.c_int32 * 1)()
+    n, nc = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert L.attn_plan_infinipipe(lens, 3, 2, 10000, 1.0, 0.0, 0.0, out, 1, ctypes.byref(n), off, 1,
+                                  ctypes.byref(nc)) == 8
+    assert n.value >= 3 and nc.value >= 2
