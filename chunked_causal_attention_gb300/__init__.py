@@ -20,7 +20,7 @@ __all__ = ["AttnError", "EXPORTS", "PLAN_UNIFORM", "PLAN_FLOPS", "PLAN_FLOPS_RES
            "attn_plan_varlen", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles", "attn_fwd_merge", "attn_bwd",
            "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_bwd_chunk", "attn_status", "attn_shape",
            "make_shape", "shape_of", "workspace", "forward", "backward", "forward_streamed", "backward_streamed",
-           "PASS_FWD", "PASS_BWD", "PASS_BWD_CHUNK", "lib", "strerror", "version"]
+           "PASS_FWD", "PASS_BWD", "PASS_BWD_CHUNK", "plan_infinipipe", "lib", "strerror", "version"]
 
 
 def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", per_chunk: bool = False):
@@ -95,3 +95,15 @@ def backward_streamed(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[f
     for c in reversed(calls):
         attn_bwd_chunk(q, k, v, o, lse, dout, c, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream)
     return dq, dk, dv, dk_acc, dv_acc
+
+
+def plan_infinipipe(seq_lens: Sequence[int], K: int, token_cap: int, cost=None):
+    """InfiniPipe Algorithm 1 (attn_plan_infinipipe) with the Eq. (1) costs
+    fitted on a GB300 (cost_gb300.json, from ``python -m
+    chunked_causal_attention_gb300.costfit fit``) unless ``cost`` =
+    (alpha1, alpha2, beta1) is given. Returns a list of calls for
+    forward_streamed / backward_streamed (packed layout of seq_lens)."""
+    if cost is None:
+        from .costfit import load_cost
+        cost = load_cost()
+    return attn_plan_infinipipe(seq_lens, K, token_cap, *cost)

@@ -160,3 +160,31 @@ def test_calls_holding_several_documents():
         check_grad(head(dq, 0, h, True), rdq, f"calls dQ h{h}")
         check_grad(head(dk, 0, h, True), rdk, f"calls dK h{h}")
         check_grad(head(dv, 0, h, True), rdv, f"calls dV h{h}")
+
+
+def test_infinipipe_plan_streamed():
+    """Calls planned by InfiniPipe Algorithm 1 (split chunks, hybrid chunks
+    holding a tail slice with short sequences, batched chunks), run one call
+    at a time, against the oracle."""
+    from oracle import infinipipe as IP
+    lens = [3000, 1, 700, 129, 2500, 40, 900, 64, 300, 1100]
+    cost = (1e-9, 2e-5, 0.0)
+    calls = cca.attn_plan_infinipipe(lens, 3, 4096, *cost)
+    want, _ = IP.plan(lens, 3, 4096, IP.Cost(*cost))
+    assert calls == [list(c) for c in want]
+    assert any(len(c) > 1 and c[0][0] > c[0][2] for c in calls)          # a hybrid chunk
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, cu[-1], 128, seed=305, packed=True))
+    o, lse = cca.forward_streamed(q, k, v, calls, packed=True)
+    dq, dk, dv, _, _ = cca.backward_streamed(q, k, v, o, lse, do, calls, packed=True)
+    torch.cuda.synchronize()
+    sc = default_scale(128)
+    for h in range(2):
+        qh, kh, vh, doh = (head(x, 0, h, True) for x in (q, k, v, do))
+        rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, sc, cu)
+        check_fwd(head(o, 0, h, True), lse_head(lse, 0, h), ro, rl, f"infinipipe h{h}")
+        check_grad(head(dq, 0, h, True), rdq, f"infinipipe dQ h{h}")
+        check_grad(head(dk, 0, h, True), rdk, f"infinipipe dK h{h}")
+        check_grad(head(dv, 0, h, True), rdv, f"infinipipe dV h{h}")
