@@ -188,9 +188,12 @@ def run_reference(args):
 
 
 def workload_config(w, args):
-    return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "tokens": w.L, "plan_chunks": w.N,
-            "plan_mode": ["uniform", "flops", "flops_resplit_edges"][w.mode], "packed": w.packed,
-            "l2": "inputs larger than L2 (1 GiB per tensor); no flush", "parallelism": f"replicas x{args.gpus}"}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "tokens": w.L, "plan_chunks": w.N,
+           "plan_mode": ["uniform", "flops", "flops_resplit_edges"][w.mode], "packed": w.packed,
+           "l2": "inputs larger than L2 (1 GiB per tensor); no flush", "parallelism": f"replicas x{args.gpus}"}
+    if w.Hkv is not None:
+        cfg["Hkv"] = w.Hkv
+    return cfg
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -219,7 +222,7 @@ def run_ours(args):
     else:
         chunks = cca.attn_plan(w.L, w.N, w.mode)
     q, k, v, do = workload_inputs(w, device=dev)
-    shape = cca.shape_of(q, w.scale, w.packed)
+    shape = cca.shape_of(q, w.scale, w.packed, k)
     o = torch.empty_like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

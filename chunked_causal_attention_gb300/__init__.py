@@ -42,7 +42,7 @@ def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", pe
 def forward(q, k, v, chunks: Sequence, scale: Optional[float] = None, packed: bool = False, ws=None, stream=None):
     """(o, lse) of chunked causal attention; q, k, v bf16 [B, H, L, D] (or packed [T, H, D])."""
     import torch
-    shape = shape_of(q, scale, packed)
+    shape = shape_of(q, scale, packed, k)
     o = torch.empty_like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
     if ws is None:
@@ -55,7 +55,7 @@ def backward(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = N
              ws=None, stream=None):
     """(dq, dk, dv) for upstream gradient dout, given the forward's o and lse."""
     import torch
-    shape = shape_of(q, scale, packed)
+    shape = shape_of(q, scale, packed, k)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if ws is None:
         ws = workspace(shape, chunks, 1, q.device)
@@ -69,7 +69,7 @@ def forward_streamed(q, k, v, chunks: Sequence, scale: Optional[float] = None, p
     chunk); each call computes its rows against the keys before them, which
     are resident in k, v."""
     import torch
-    shape = shape_of(q, scale, packed)
+    shape = shape_of(q, scale, packed, k)
     o = torch.empty_like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
     calls = [c if isinstance(c[0], (list, tuple)) else [c] for c in chunks]
@@ -85,7 +85,7 @@ def backward_streamed(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[f
     ``chunks`` as forward_streamed), with fp32 dK/dV accumulators shared by
     the calls (attn_bwd_chunk). Returns (dq, dk, dv, dk_acc, dv_acc)."""
     import torch
-    shape = shape_of(q, scale, packed)
+    shape = shape_of(q, scale, packed, k)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     # fp32 accumulators at the same element offsets as k and v
     dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=k.device).zero_()

@@ -51,7 +51,8 @@ class attn_chunk(ctypes.Structure):
 class attn_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("D", ctypes.c_int64),
                 ("sb", ctypes.c_int64), ("st", ctypes.c_int64), ("sh", ctypes.c_int64),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float),
+                ("Hkv", ctypes.c_int64), ("sb_kv", ctypes.c_int64), ("st_kv", ctypes.c_int64), ("sh_kv", ctypes.c_int64)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -168,19 +169,30 @@ def attn_plan_infinipipe(seq_lens: Sequence[int], K: int, token_cap: int, alpha1
 
 # ------------------------------------------------------------------ shapes
 
-def make_shape(B, H, T, D, sb, st, sh, scale) -> attn_shape:
-    return attn_shape(B, H, T, D, sb, st, sh, float(scale))
+def make_shape(B, H, T, D, sb, st, sh, scale, Hkv=0, sb_kv=0, st_kv=0, sh_kv=0) -> attn_shape:
+    return attn_shape(B, H, T, D, sb, st, sh, float(scale), Hkv, sb_kv, st_kv, sh_kv)
 
 
-def shape_of(x, scale: Optional[float] = None, packed: bool = False) -> attn_shape:
-    """attn_shape of a torch tensor: dense [B, H, L, D] or packed [T, H, D]."""
-    D = x.shape[-1]
-    sc = (1.0 / D ** 0.5) if scale is None else scale
+def _bths(x, packed: bool):
+    """(B, heads, T, sb, st, sh) of a dense [B, H, L, D] or packed [T, H, D] tensor."""
     if packed:
         T, H, _ = x.shape
-        return make_shape(1, H, T, D, x.stride(0) * T, x.stride(0), x.stride(1), sc)
+        return 1, H, T, x.stride(0) * T, x.stride(0), x.stride(1)
     B, H, L, _ = x.shape
-    return make_shape(B, H, L, D, x.stride(0), x.stride(2), x.stride(1), sc)
+    return B, H, L, x.stride(0), x.stride(2), x.stride(1)
+
+
+def shape_of(x, scale: Optional[float] = None, packed: bool = False, k=None) -> attn_shape:
+    """attn_shape of a query tensor: dense [B, H, L, D] or packed [T, H, D].
+    Given k with fewer heads than x (grouped key/value heads), the shape also
+    carries k's head count and strides (used for k, v, dk, dv)."""
+    D = x.shape[-1]
+    sc = (1.0 / D ** 0.5) if scale is None else scale
+    B, H, T, sb, st, sh = _bths(x, packed)
+    if k is None or k.shape == x.shape and k.stride() == x.stride():
+        return make_shape(B, H, T, D, sb, st, sh, sc)
+    _, Hkv, _, sbk, stk, shk = _bths(k, packed)
+    return make_shape(B, H, T, D, sb, st, sh, sc, Hkv, sbk, stk, shk)
 
 
 def attn_workspace_size(shape: attn_shape, chunks, pass_: int) -> int:

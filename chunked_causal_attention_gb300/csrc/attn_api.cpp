@@ -29,6 +29,17 @@ int check_shape(const attn_shape* s, Geom* g) {
     if ((s->sb % 8) || (s->st % 8) || (s->sh % 8)) return ATTN_E_ALIGN;
     g->B = (int32_t)s->B; g->H = (int32_t)s->H; g->T = (int32_t)s->T; g->D = (int32_t)s->D;
     g->sb = s->sb; g->st = s->st; g->sh = s->sh; g->scale = s->scale;
+    if (s->Hkv < 0 || s->Hkv > s->H) return ATTN_E_INVAL;
+    if (s->Hkv == 0) {
+        g->Hkv = g->H;
+        g->sb_kv = g->sb; g->st_kv = g->st; g->sh_kv = g->sh;
+    } else {
+        if (s->H % s->Hkv) return ATTN_E_INVAL;
+        if (s->sb_kv <= 0 || s->st_kv <= 0 || s->sh_kv <= 0) return ATTN_E_INVAL;
+        if ((s->sb_kv % 8) || (s->st_kv % 8) || (s->sh_kv % 8)) return ATTN_E_ALIGN;
+        g->Hkv = (int32_t)s->Hkv;
+        g->sb_kv = s->sb_kv; g->st_kv = s->st_kv; g->sh_kv = s->sh_kv;
+    }
     return ATTN_OK;
 }
 

@@ -63,10 +63,23 @@ struct RowSeg {
     int32_t ws_row0, t0, R;
 };
 
+// Shape of q/o/dout/dq (B, H, T, D with strides sb, st, sh) and of the
+// key/value tensors k/v/dk/dv (Hkv heads, strides sb_kv, st_kv, sh_kv); query
+// head h reads key/value head h / (H / Hkv).
 struct Geom {
     int32_t B, H, T, D;
     int64_t sb, st, sh;
     float scale;
+    int32_t Hkv;
+    int64_t sb_kv, st_kv, sh_kv;
+    int32_t group() const { return H / Hkv; }
+    // the key/value tensors' geometry in the query fields (for tensor maps)
+    Geom kv() const {
+        Geom k = *this;
+        k.H = Hkv;
+        k.sb = sb_kv; k.st = st_kv; k.sh = sh_kv;
+        return k;
+    }
 };
 
 struct FwdArgs {

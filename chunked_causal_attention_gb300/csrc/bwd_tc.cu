@@ -9,7 +9,9 @@
 // chunk's rows, and dK/dV are added into fp32 accumulators that the chunks of a
 // document share when run in reverse order. Persistent CTAs take items
 // head-major (all CTAs on one head at a time), so the head's Q/dO tiles and
-// dQ accumulator rows are reused from L2.
+// dQ accumulator rows are reused from L2. With grouped key/value heads (GQA/MQA)
+// an item is a key tile of one key/value head and walks the query blocks of
+// each of its H / Hkv query heads in turn, so dK/dV collect the group's sum.
 //
 // Warp roles (16 warps):
 //   warp 0       TMA producer: K, V once per item; Q and dO of a query block into
@@ -160,7 +162,8 @@ template <int D>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                  const __grid_constant__ CUtensorMap tmdq, const BwdArgs a, const TcMaps mp, const int32_t n_work) {
+                  const __grid_constant__ CUtensorMap tmdq, const BwdArgs a, const TcMaps mp, const TcMaps mpkv,
+                  const int32_t n_work) {
     using LY = BwdTcLayout<D>;
     constexpr uint32_t kColDK = kColDV + D;
     extern __shared__ uint8_t smem_raw[];
@@ -174,7 +177,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     float* s_nd = reinterpret_cast<float*>(sm + LY::ND_OFF);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int BH = a.g.B * a.g.H;
+    const int BHKV = a.g.B * a.g.Hkv;            // work items run over (key tile, batch, key/value head)
+    const int G = a.g.H / a.g.Hkv;               // query heads per key/value head
 
     if (tid == 0) {
         mbar_init(bar(LY::B_KVFULL), 1);
@@ -212,25 +216,26 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             uint32_t qc = 0, ic = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < n_work && !a.stall && ok && !*abort_flag; w += gridDim.x, ++ic) {
-                int32_t it, bh;
-                decode_work(w, a.n_items, BH, a.group, it, bh);
+                int32_t it, bkv;
+                decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
-                const int b = bh / a.g.H, h = bh % a.g.H;
+                const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
                 ok = mbar_wait(bar(LY::B_KVEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 mbar_expect_tx(bar(LY::B_KVFULL), 2 * LY::TILE);
-                load_tile_b<D>(sbase + LY::K_OFF, &tmk, bar(LY::B_KVFULL), mp, item.j0, h, b);
-                load_tile_b<D>(sbase + LY::V_OFF, &tmv, bar(LY::B_KVFULL), mp, item.j0, h, b);
+                load_tile_b<D>(sbase + LY::K_OFF, &tmk, bar(LY::B_KVFULL), mpkv, item.j0, hk, b);
+                load_tile_b<D>(sbase + LY::V_OFF, &tmv, bar(LY::B_KVFULL), mpkv, item.j0, hk, b);
                 const int nq = (item.q_end - item.q_lo + 127) / 128;
-                for (int i = 0; i < nq; ++i, ++qc) {
+                for (int blk = 0; blk < G * nq; ++blk, ++qc) {
+                    const int g = blk / nq, i = blk - g * nq;
                     const uint32_t s = qc & 1;
                     ok = mbar_wait(bar(LY::B_QEMPTY + s), ((qc >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_QFULL + s), LY::STAGE);
                     const int row = item.q_lo + (nq - 1 - i) * 128;
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
-                    load_tile_b<D>(st, &tmq, bar(LY::B_QFULL + s), mp, row, h, b);
-                    load_tile_b<D>(st + LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, h, b);
+                    load_tile_b<D>(st, &tmq, bar(LY::B_QFULL + s), mp, row, hk * G + g, b);
+                    load_tile_b<D>(st + LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, hk * G + g, b);
                 }
             }
         }
@@ -244,14 +249,14 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             uint32_t qc = 0, ic = 0, gb = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
-                int32_t it, bh;
-                decode_work(w, a.n_items, BH, a.group, it, bh);
+                int32_t it, bkv;
+                decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
                 const int nq = (item.q_end - item.q_lo + 127) / 128;
                 ok = mbar_wait(bar(LY::B_KVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
-                for (int i = 0; i < nq; ++i, ++qc, ++gb) {
+                for (int blk = 0; blk < G * nq; ++blk, ++qc, ++gb) {
                     const uint32_t s = qc & 1;
                     ok = mbar_wait(bar(LY::B_QFULL + s), (qc >> 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                                kk > 0);
                     }
                     mma_commit(bar(LY::B_SDP));
-                    if (i == 0) {
+                    if (blk == 0) {
                         ok = mbar_wait(bar(LY::B_DKDVFREE), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                     }
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int kk = 2 * c + h;
-                            const uint32_t acc = (i > 0 || n > 0 || h > 0) ? 1u : 0u;
+                            const uint32_t acc = (blk > 0 || n > 0 || h > 0) ? 1u : 0u;
                             mma_ts(tmem + kColDV, tmem + kColS + 32 * c + 8 * h,
                                    sdesc_sw128(o0 + kk * 2048, 16384, 1024), id_g, acc);
                             mma_ts(tmem + kColDK, tmem + kColDP + 32 * c + 8 * h,
@@ -324,22 +329,27 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         const bool stage_l = krow < 64;
         float* stage_dst = (stage_l ? s_nl : s_nd) + 64 * grp + (krow & 63);
         for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
-            int32_t it, bh;
-            decode_work(w, a.n_items, BH, a.group, it, bh);
+            int32_t it, bkv;
+            decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];
+            const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
             const int key = item.j0 + krow;
-            // src[t] for a token t: LSE (all tokens) or delta (workspace row t + row_off)
-            const float* src = stage_l ? a.lse + (int64_t)bh * a.g.T : a.delta + (int64_t)bh * a.rows + item.row_off;
+            // value staged for block blk: src[t] of its query head, t = the block's
+            // row 64*grp + (krow & 63); LSE (all tokens) or delta (workspace row t + row_off)
+            auto fetch = [&](int blk) -> float {
+                const int g = blk / nq, i = blk - g * nq;
+                const int64_t bhq = (int64_t)b * a.g.H + hk * G + g;
+                const int q = item.q_lo + (nq - 1 - i) * 128 + 64 * grp + (krow & 63);
+                if (q >= item.q_end) return 0.f;
+                return stage_l ? a.lse[bhq * a.g.T + q] : a.delta[bhq * a.rows + item.row_off + q];
+            };
             const float mul = stage_l ? -kLog2e : -1.f;
             // raw value of the next block, scaled only when it is staged, so the
             // load's latency is not waited for until then
-            float next = 0.f;
-            {
-                const int q = item.q_lo + (nq - 1) * 128 + 64 * grp + (krow & 63);
-                if (q < item.q_end) next = src[q];
-            }
-            for (int i = 0; i < nq; ++i, ++gb) {
+            float next = fetch(0);
+            for (int blk = 0; blk < G * nq; ++blk, ++gb) {
+                const int i = blk - (blk / nq) * nq;
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;  // query blocks walked from the last one down
                 if (*abort_flag) {
                     ok = false;
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 named_sync(1 + grp, 128);
                 *stage_dst = next * mul;
                 named_sync(1 + grp, 128);
-                if (i + 1 < nq) next = src[i0 - 128 + 64 * grp + (krow & 63)];
+                if (blk + 1 < G * nq) next = fetch(blk + 1);
                 ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 if (gb > 0) {
@@ -371,8 +381,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             ok = mbar_wait(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
             if (!ok) break;
             tc_fence_after();
-            const int b_ = bh / a.g.H, h_ = bh % a.g.H;
-            const int64_t roff = (int64_t)b_ * a.g.sb + (int64_t)h_ * a.g.sh + (int64_t)key * a.g.st;
+            const int64_t roff = (int64_t)b * a.g.sb_kv + (int64_t)hk * a.g.sh_kv + (int64_t)key * a.g.st_kv;
             const bool live = key < item.j1;
             const uint32_t col = grp == 0 ? kColDK : kColDV;
             const float gmul = grp == 0 ? a.g.scale : 1.f;
@@ -425,12 +434,15 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         uint32_t gb = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x) {
-            int32_t it, bh;
-            decode_work(w, a.n_items, BH, a.group, it, bh);
+            int32_t it, bkv;
+            decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];
+            const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
-            for (int i = 0; i < nq; ++i, ++gb) {
+            for (int blk = 0; blk < G * nq; ++blk, ++gb) {
+                const int g = blk / nq, i = blk - g * nq;
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;
+                const int bhq = b * a.g.H + hk * G + g;      // the block's query head (dQ accumulator)
                 const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
                 uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
@@ -466,7 +478,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc)
-                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 + item.row_off, bh);
+                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 + item.row_off, bhq);
                     bulk_commit();
                     bulk_wait_read_all();
                     mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage
@@ -497,18 +509,20 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 template <int D>
 cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq;
-    TcMaps mp{1, 2, 3};
-    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, a.g, mp) || !make_tile_map(&mv, a.v, a.g, mp) ||
-        !make_tile_map(&mdo, a.dout, a.g, mp) || !make_dq_acc_map(&mdq, a.dq_acc, a.g, a.rows))
+    TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
+    const Geom gkv = a.g.kv();
+    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, gkv, mpkv) ||
+        !make_tile_map(&mv, a.v, gkv, mpkv) || !make_tile_map(&mdo, a.dout, a.g, mp) ||
+        !make_dq_acc_map(&mdq, a.dq_acc, a.g, a.rows))
         return cudaErrorInvalidValue;
-    const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
+    const int64_t work = (int64_t)a.n_items * a.g.B * a.g.Hkv;
     if (work <= 0) return cudaSuccess;
     if (work > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = BwdTcLayout<D>::ALLOC;
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_tc_kernel<D><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, (int32_t)work);
+    bwd_tc_kernel<D><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
     return cudaGetLastError();
 }
 

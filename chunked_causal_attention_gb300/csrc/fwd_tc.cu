@@ -3,7 +3,9 @@
 // Persistent CTAs walk the cost-sorted work list (128 query rows x one key
 // range x one (batch, head)). Warp roles:
 //   warp 0      TMA producer: Q tile once per item; K and V tiles of 128 keys
-//               through two-stage rings (128-byte swizzled, 64-column boxes).
+//               through two-stage rings (128-byte swizzled, 64-column boxes),
+//               from the key/value head of the item's query head (grouped
+//               heads: h / (H / Hkv)).
 //   warp 1      MMA issuer (one thread) and TMEM owner:
 //                 S_j   = Q K_j^T        (both operands K-major in shared memory)
 //                 O    += P_j V_j        (P_j from TMEM, V_j MN-major in shared memory)
@@ -82,7 +84,8 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 template <int D>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const FwdArgs a, const TcMaps mp, const int32_t n_work) {
+                  const __grid_constant__ CUtensorMap tmv, const FwdArgs a, const TcMaps mp, const TcMaps mpkv,
+                  const int32_t n_work) {
     using LY = FwdTcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
                 const int b = bh / a.g.H, h = bh % a.g.H;
+                const int hk = h / (a.g.H / a.g.Hkv);
                 if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns)) break;
                 mbar_expect_tx(bar(LY::B_QFULL), LY::TILE);
                 load_tile<D>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
@@ -147,12 +151,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ok = mbar_wait(bar(LY::B_KEMPTY + ks), ((kc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_KFULL + ks), LY::TILE);
-                    load_tile<D>(sbase + LY::K_OFF + ks * LY::TILE, &tmk, bar(LY::B_KFULL + ks), mp, row, h, b);
+                    load_tile<D>(sbase + LY::K_OFF + ks * LY::TILE, &tmk, bar(LY::B_KFULL + ks), mpkv, row, hk, b);
                     ++kc;
                     ok = mbar_wait(bar(LY::B_VEMPTY + vs), ((vc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE);
-                    load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mp, row, h, b);
+                    load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mpkv, row, hk, b);
                     ++vc;
                 }
                 if (!ok) break;
@@ -403,8 +407,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv;
-    TcMaps mp{1, 2, 3};
-    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, a.g, mp) || !make_tile_map(&mv, a.v, a.g, mp))
+    TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
+    const Geom gkv = a.g.kv();
+    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, gkv, mpkv) ||
+        !make_tile_map(&mv, a.v, gkv, mpkv))
         return cudaErrorInvalidValue;
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
     if (work <= 0) return cudaSuccess;
@@ -413,7 +419,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    fwd_tc_kernel<D><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, (int32_t)work);
+    fwd_tc_kernel<D><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, mpkv, (int32_t)work);
     return cudaGetLastError();
 }
 

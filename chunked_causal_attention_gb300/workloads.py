@@ -17,6 +17,9 @@ no dataset is available here, so all tensors are i.i.d. N(0, 1) cast to bf16):
                  real-world length distribution, Fig. 1(b)); documents longer
                  than 16K are cut into FLOPs-balanced chunks.
 * ``13b_1m``     B=1 H=40 D=128 L=1048576, FLOPS plan N=64.
+* ``gqa_128k``   B=1 H=32 with 8 key/value heads (grouped-query attention,
+                 4 query heads per key/value head), D=128 L=131072, the same
+                 plan as 7b_128k.
 """
 from __future__ import annotations
 
@@ -45,6 +48,7 @@ class Workload:
     packed: bool = False
     max_chunk_tokens: int = 16384
     doc_lens: Optional[List[int]] = field(default=None, compare=False)
+    Hkv: Optional[int] = None  # key/value heads (grouped-query attention); None: H
 
     @property
     def scale(self) -> float:
@@ -90,6 +94,7 @@ WORKLOADS = {
     "packed_256k": Workload("packed_256k", 1, 32, 128, 262144, mode=PLAN_FLOPS, seed=1237, packed=True,
                             max_chunk_tokens=16384, doc_lens=skewed_doc_lengths()),
     "13b_1m": Workload("13b_1m", 1, 40, 128, 1048576, N=64, mode=PLAN_FLOPS, seed=1238),
+    "gqa_128k": Workload("gqa_128k", 1, 32, 128, 131072, N=16, mode=PLAN_FLOPS_RESPLIT_EDGES, seed=1239, Hkv=8),
 }
 
 
@@ -100,13 +105,16 @@ def randn_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
-def make_inputs(B: int, H: int, L: int, D: int, seed: int, device="cpu", packed: bool = False):
-    """(q, k, v, do) bf16 tensors; dense layout [B, H, L, D], packed [L, H, D].
+def make_inputs(B: int, H: int, L: int, D: int, seed: int, device="cpu", packed: bool = False,
+                Hkv: Optional[int] = None):
+    """(q, k, v, do) bf16 tensors; dense layout [B, H, L, D], packed [L, H, D];
+    k and v have Hkv heads when given (grouped key/value heads).
 
     Each tensor has its own stream: seeds seed*4 + {0,1,2,3}."""
-    shape = (L, H, D) if packed else (B, H, L, D)
-    return tuple(randn_bf16(shape, seed * 4 + i, device) for i in range(4))
+    hk = H if Hkv is None else Hkv
+    shapes = [(L, h, D) if packed else (B, h, L, D) for h in (H, hk, hk, H)]
+    return tuple(randn_bf16(shapes[i], seed * 4 + i, device) for i in range(4))
 
 
 def workload_inputs(w: Workload, device="cpu"):
-    return make_inputs(w.B, w.H, w.L, w.D, w.seed, device=device, packed=w.packed)
+    return make_inputs(w.B, w.H, w.L, w.D, w.seed, device=device, packed=w.packed, Hkv=w.Hkv)

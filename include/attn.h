@@ -32,6 +32,11 @@
  *     strides for all eight tensors. Dense [B, H, L, D]: sb = H*L*D, sh = L*D,
  *     st = D. Packed [T, H, D] (B = 1): st = H*D, sh = D.
  *     Base pointers must be 16-byte aligned and sb, st, sh multiples of 8.
+ *   - Grouped key/value heads (GQA/MQA): with Hkv > 0 in the shape, k, v, dk,
+ *     dv (and the fp32 accumulators of attn_bwd_chunk) have Hkv heads and
+ *     their own strides sb_kv, st_kv, sh_kv; query head h reads key/value head
+ *     h / (H / Hkv), and the gradient of a key/value head is the sum over its
+ *     H / Hkv query heads. Hkv = 0 means Hkv = H with the query strides.
  *   - lse: fp32, [B][H][T] contiguous, natural log.
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Compute calls only enqueue work and return before it completes.
@@ -83,6 +88,8 @@ typedef struct {
     int64_t B, H, T, D;   /* batch rows, heads, tokens per row, head dim     */
     int64_t sb, st, sh;   /* element strides of batch, token, head           */
     float   scale;        /* softmax scale; usually 1/sqrt(D)                */
+    int64_t Hkv;          /* key/value heads (H % Hkv == 0); 0: Hkv = H     */
+    int64_t sb_kv, st_kv, sh_kv;   /* strides of k, v, dk, dv when Hkv > 0  */
 } attn_shape;
 
 /* ---- planning (host only, integer-exact; never touches the GPU) -------- */

@@ -301,6 +301,26 @@ def chunked_forward(q, k, v, chunks: Sequence[Tuple[int, int, int, int]], scale:
     return O, LSE
 
 
+def grouped_backward(qs, k, v, dos, scale: float, cu_seqlens=None, row_block: int = 512):
+    """Grouped key/value heads (GQA/MQA): the query heads in ``qs`` (each
+    [T, D], upstream gradients in ``dos``) all read the one key/value head
+    (k, v). Each query head is plain attention against (k, v); the gradient of
+    the shared k and v is the sum of the per-head gradients (the chain rule
+    for a tensor used by several heads). Returns (dQ per head, dK, dV, O per
+    head, LSE per head)."""
+    dqs, Os, Ls = [], [], []
+    dk = np.zeros_like(_f64(k))
+    dv = np.zeros_like(_f64(v))
+    for q, do in zip(qs, dos):
+        dq, dk_h, dv_h, O, L = backward(q, k, v, do, scale, cu_seqlens, row_block)
+        dqs.append(dq)
+        Os.append(O)
+        Ls.append(L)
+        dk += dk_h
+        dv += dv_h
+    return dqs, dk, dv, Os, Ls
+
+
 def chunk_backward(q, k, v, do, qb: int, qe: int, cb: int, scale: float, row_block: int = 512):
     """Contributions of the query rows of ONE chunk, [qb, qe) with context
     starting at cb (the document start), to the gradients: the definition's

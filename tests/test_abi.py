@@ -124,6 +124,22 @@ def test_workspace_partials_sized_for_split_rows():
     assert extra >= 2 * rows * 32 * (128 + 1) * 4
 
 
+def test_grouped_heads_shape_validation():
+    """Hkv must divide H; key/value strides follow the same alignment rule."""
+    ch = cca.attn_plan(1024, 4, 0)
+    ok = cca.make_shape(1, 8, 1024, 64, 8 * 1024 * 64, 64, 1024 * 64, 0.1, 2, 2 * 1024 * 64, 64, 1024 * 64)
+    assert cca.attn_workspace_size(ok, ch, 1) > 0
+    for bad, st in [((3, 3 * 1024 * 64, 64, 1024 * 64), 1),        # 8 % 3 != 0
+                    ((16, 16 * 1024 * 64, 64, 1024 * 64), 1),      # more key/value heads than query heads
+                    ((2, 2 * 1024 * 64, 60, 1024 * 64), 2),        # key/value token stride not a multiple of 8
+                    ((2, 0, 64, 1024 * 64), 1),
+                    ((-1, 0, 0, 0), 1)]:
+        s = cca.make_shape(1, 8, 1024, 64, 8 * 1024 * 64, 64, 1024 * 64, 0.1, *bad)
+        with pytest.raises(cca.AttnError) as e:
+            cca.attn_workspace_size(s, ch, 0)
+        assert e.value.status == st, bad
+
+
 def test_compute_calls_reject_bad_arguments_on_host():
     """Validation happens before any CUDA call, so these run without a GPU."""
     L = cca.lib()

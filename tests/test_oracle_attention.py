@@ -299,3 +299,37 @@ def test_chunk_backward_streamed_equals_full(mode):
         np.testing.assert_allclose(gq, dq, atol=1e-12)
         np.testing.assert_allclose(adk, dk, atol=1e-12)
         np.testing.assert_allclose(adv, dv, atol=1e-12)
+
+
+# ---------------------------------------------------- grouped key/value heads
+
+@pytest.mark.parametrize("G,cu", [(4, None), (3, [0, 50, 51, 120]), (1, None)])
+def test_grouped_backward_matches_autograd(G, cu):
+    """GQA/MQA: G query heads share one key/value head. Library pin: torch
+    float64 SDPA of each query head against the shared K, V tensors (leaf
+    tensors with requires_grad), whose .grad autograd sums over the heads."""
+    T, D, sc = 120, 8, 0.3
+    qs = [rand((T, D), 200 + g) for g in range(G)]
+    dos = [rand((T, D), 300 + g) for g in range(G)]
+    k, v = rand((T, D), 401), rand((T, D), 402)
+    dqs, dk, dv, Os, Ls = A.grouped_backward(qs, k, v, dos, sc, cu)
+    K = torch.tensor(k, requires_grad=True)
+    V = torch.tensor(v, requires_grad=True)
+    mask = torch.zeros(T, T, dtype=torch.bool)
+    docs = cu or [0, T]
+    for s_, e_ in zip(docs[:-1], docs[1:]):
+        mask[s_:e_, s_:e_] = torch.tril(torch.ones(e_ - s_, e_ - s_, dtype=torch.bool))
+    total = 0
+    Qs = []
+    for g in range(G):
+        Q = torch.tensor(qs[g], requires_grad=True)
+        Qs.append(Q)
+        O = torch.nn.functional.scaled_dot_product_attention(Q[None, None], K[None, None], V[None, None],
+                                                             attn_mask=mask, scale=sc)[0, 0]
+        np.testing.assert_allclose(O.detach().numpy(), Os[g], atol=1e-12)
+        total = total + (O * torch.tensor(dos[g])).sum()
+    total.backward()
+    for g in range(G):
+        np.testing.assert_allclose(Qs[g].grad.numpy(), dqs[g], atol=1e-11)
+    np.testing.assert_allclose(K.grad.numpy(), dk, atol=1e-11)
+    np.testing.assert_allclose(V.grad.numpy(), dv, atol=1e-11)
