@@ -80,13 +80,12 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 template <int D>
 __device__ __forceinline__ void load_tile_b(uint32_t dst, const CUtensorMap* map, uint32_t bar, const TcMaps& mp,
                                             int row, int h, int b) {
-    int c[4];
-    c[0] = 0;
-    c[mp.pos_t] = row;
-    c[mp.pos_h] = h;
-    c[mp.pos_b] = b;
+    // coordinates of map axes 1..3 (token, head, batch in stride order), by selects
+    const int c1 = mp.pos_t == 1 ? row : (mp.pos_h == 1 ? h : b);
+    const int c2 = mp.pos_t == 2 ? row : (mp.pos_h == 2 ? h : b);
+    const int c3 = mp.pos_t == 3 ? row : (mp.pos_h == 3 ? h : b);
 #pragma unroll
-    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c[1], c[2], c[3]);
+    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c1, c2, c3);
 }
 
 // Softmax gradient of one query block for one warpgroup (query columns
@@ -158,7 +157,10 @@ __device__ __forceinline__ void sg_block(uint32_t tm, int grp, int krow, int key
     }
 }
 
-template <int D>
+// GROUPED: key/value heads shared by several query heads. The ungrouped
+// instantiation has G = 1 at compile time, which keeps the per-block walk of
+// the softmax-gradient warps as light as it was before grouping existed.
+template <int D, bool GROUPED>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int BHKV = a.g.B * a.g.Hkv;            // work items run over (key tile, batch, key/value head)
-    const int G = a.g.H / a.g.Hkv;               // query heads per key/value head
+    const int G = GROUPED ? a.g.H / a.g.Hkv : 1;  // query heads per key/value head
 
     if (tid == 0) {
         mbar_init(bar(LY::B_KVFULL), 1);
@@ -335,21 +337,24 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
             const int key = item.j0 + krow;
-            // value staged for block blk: src[t] of its query head, t = the block's
-            // row 64*grp + (krow & 63); LSE (all tokens) or delta (workspace row t + row_off)
-            auto fetch = [&](int blk) -> float {
-                const int g = blk / nq, i = blk - g * nq;
+            // src[t] for a token t of query head hk*G + g: LSE (all tokens) or delta
+            // (workspace row t + row_off)
+            auto src_of = [&](int g) -> const float* {
                 const int64_t bhq = (int64_t)b * a.g.H + hk * G + g;
-                const int q = item.q_lo + (nq - 1 - i) * 128 + 64 * grp + (krow & 63);
-                if (q >= item.q_end) return 0.f;
-                return stage_l ? a.lse[bhq * a.g.T + q] : a.delta[bhq * a.rows + item.row_off + q];
+                return stage_l ? a.lse + bhq * a.g.T : a.delta + bhq * a.rows + item.row_off;
             };
+            const float* src = src_of(0);
+            const int qoff = 64 * grp + (krow & 63);      // the block row this thread stages
             const float mul = stage_l ? -kLog2e : -1.f;
             // raw value of the next block, scaled only when it is staged, so the
             // load's latency is not waited for until then
-            float next = fetch(0);
+            float next = 0.f;
+            {
+                const int q = item.q_lo + (nq - 1) * 128 + qoff;
+                if (q < item.q_end) next = src[q];
+            }
+            int i = 0, g = 0;                              // the block: query head hk*G + g, i-th from the top
             for (int blk = 0; blk < G * nq; ++blk, ++gb) {
-                const int i = blk - (blk / nq) * nq;
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;  // query blocks walked from the last one down
                 if (*abort_flag) {
                     ok = false;
@@ -358,7 +363,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 named_sync(1 + grp, 128);
                 *stage_dst = next * mul;
                 named_sync(1 + grp, 128);
-                if (blk + 1 < G * nq) next = fetch(blk + 1);
+                if (i + 1 < nq) {
+                    next = src[i0 - 128 + qoff];           // the next block down, same query head
+                } else if (g + 1 < G) {
+                    src = src_of(g + 1);                   // the top block of the group's next query head
+                    const int q = item.q_lo + (nq - 1) * 128 + qoff;
+                    next = q < item.q_end ? src[q] : 0.f;
+                }
                 ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 if (gb > 0) {
@@ -375,6 +386,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     sg_block<true>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
                 else
                     sg_block<false>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
+                if (++i == nq) {
+                    i = 0;
+                    ++g;
+                }
             }
             if (!ok) break;
             // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16)
@@ -439,10 +454,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const BwdItem item = a.items[it];
             const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
+            int i = 0, bhq = b * a.g.H + hk * G;             // the block's index and query head (dQ rows)
             for (int blk = 0; blk < G * nq; ++blk, ++gb) {
-                const int g = blk / nq, i = blk - g * nq;
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;
-                const int bhq = b * a.g.H + hk * G + g;      // the block's query head (dQ accumulator)
                 const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
                 uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
                 ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
@@ -483,6 +497,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     bulk_wait_read_all();
                     mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage
                 }
+                if (++i == nq) {
+                    i = 0;
+                    ++bhq;
+                }
             }
         }
         if (qrow == 0) bulk_wait_all();
@@ -506,7 +524,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, bool GROUPED>
 cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
@@ -519,17 +537,19 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     if (work <= 0) return cudaSuccess;
     if (work > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = BwdTcLayout<D>::ALLOC;
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_tc_kernel<D, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_tc_kernel<D><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
+    bwd_tc_kernel<D, GROUPED><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s) {
-    return a.g.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+    if (a.g.Hkv != a.g.H) return a.g.D == 128 ? launch_d<128, true>(a, s) : launch_d<64, true>(a, s);
+    return a.g.D == 128 ? launch_d<128, false>(a, s) : launch_d<64, false>(a, s);
 }
 
 }  // namespace attn

@@ -65,20 +65,15 @@ struct FwdTcLayout {
     static constexpr size_t ALLOC = (size_t)BYTES + 1024;      // slack for 1024-byte alignment
 };
 
-__device__ __forceinline__ void tile_coords(const TcMaps& mp, int row, int h, int b, int (&c)[4]) {
-    c[0] = 0;
-    c[mp.pos_t] = row;
-    c[mp.pos_h] = h;
-    c[mp.pos_b] = b;
-}
-
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, const TcMaps& mp,
                                           int row, int h, int b) {
-    int c[4];
-    tile_coords(mp, row, h, b, c);
+    // coordinates of map axes 1..3 (token, head, batch in stride order), by selects
+    const int c1 = mp.pos_t == 1 ? row : (mp.pos_h == 1 ? h : b);
+    const int c2 = mp.pos_t == 2 ? row : (mp.pos_h == 2 ? h : b);
+    const int c3 = mp.pos_t == 3 ? row : (mp.pos_h == 3 ? h : b);
 #pragma unroll
-    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c[1], c[2], c[3]);
+    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c1, c2, c3);
 }
 
 template <int D>
