@@ -282,16 +282,18 @@ def chunked_forward(q, k, v, chunks: Sequence[Tuple[int, int, int, int]], scale:
                     kv_block: Optional[int] = None):
     """The chunked method: for each chunk (q_begin, q_end, ctx_begin, kv_split)
     the chunk's queries attend to the resident keys [ctx_begin, q_end); with a
-    re-split point m the key range is split into [ctx_begin, m) and [m, q_end)
-    and the two partials are merged by LSE. ``kv_block`` further cuts every
+    re-split point m > 0 the key range is split into [ctx_begin, m) and
+    [m, q_end), with kv_split = -P into P parts of equal visible-pair count
+    (``oracle.plan.key_ranges``), and the partials are merged by LSE. ``kv_block`` further cuts every
     key range into blocks of that many keys, each contributing one partial
     (the ring's one-block-per-hop accumulation)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     T = q.shape[0]
     O = np.zeros((T, v.shape[1]))
     LSE = np.full(T, NEG_INF)
+    from oracle.plan import key_ranges
     for qb, qe, cb, m in chunks:
-        ranges = [(cb, m), (m, qe)] if m else [(cb, qe)]
+        ranges = key_ranges((qb, qe, cb, m))
         if kv_block:
             ranges = [(a, min(a + kv_block, b)) for lo, b in ranges for a in range(lo, b, kv_block)]
         parts = [partial(q, k, v, qb, qe, lo, hi, scale) for lo, hi in ranges]

@@ -28,6 +28,15 @@ Readings taken where the pages leave a step open (stated in the design doc):
 * Re-split point m = q_begin + 128*floor((q_end - q_begin)/256 + 1/2); the
   split is along the key/value range (parts [ctx_begin, m) and [m, q_end));
   no split when m does not fall strictly inside (q_begin, q_end).
+* Re-split into P parts (kv_split = -P): the chunk's key range [ctx_begin,
+  q_end) is cut into P parts carrying equal numbers of visible (query, key)
+  pairs of the chunk's queries; boundary k_p is the multiple of 128 (counted
+  from ctx_begin) nearest to the point where the pairs of keys before it reach
+  p/P of the total (ties up); boundaries that collapse are an error. SPPO
+  Table 3 (multiplexed partition): the SP range of the edge subsequences
+  shrinks by one device per subsequence away from each pipeline end, read as
+  chunk i and chunk N-1-i of N getting PP - i parts (the largest valid count
+  up to that), for PP pipeline stages.
 * Varlen: a document of length L_d is cut into ceil(L_d / max_chunk_tokens)
   chunks with the same rule measured from the document start; every chunk of a
   document has ctx_begin = document start. Empty documents give no chunk. In
@@ -130,6 +139,70 @@ def plan_varlen(cu_seqlens: Sequence[int], max_chunk_tokens: int, mode: int) -> 
             chunks.append([s + b[i], s + b[i + 1], s, 0])
     if mode == FLOPS_RESPLIT_EDGES:
         _apply_resplit(chunks)
+    return [tuple(c) for c in chunks]
+
+
+def key_pairs_before(q_begin: int, q_end: int, ctx_begin: int, K: int) -> int:
+    """Visible (query, key) pairs of a chunk's queries [q_begin, q_end) with the
+    keys in [ctx_begin, K): a context key is seen by every query, key j inside
+    the chunk by the queries t >= j."""
+    n = q_end - q_begin
+    A = min(K, q_begin) - ctx_begin
+    B = max(0, K - q_begin)
+    return A * n + B * n - B * (B - 1) // 2
+
+
+def resplit_boundaries(q_begin: int, q_end: int, ctx_begin: int, P: int) -> List[int]:
+    """Key-range boundaries ctx_begin = k_0 < k_1 < ... < k_P = q_end of a chunk
+    re-split into P parts of equal visible-pair count (nearest multiple of 128
+    from ctx_begin, ties up)."""
+    if P < 2:
+        raise PlanError("a re-split needs at least two parts")
+    W = key_pairs_before(q_begin, q_end, ctx_begin, q_end)
+    k = [ctx_begin]
+    for p in range(1, P):
+        m = 0
+        while True:
+            half = ctx_begin + TILE * (m + 1) - TILE // 2
+            if half > q_end or P * key_pairs_before(q_begin, q_end, ctx_begin, half) > p * W:
+                break
+            m += 1
+        k.append(ctx_begin + TILE * m)
+    k.append(q_end)
+    if any(not k[i] < k[i + 1] for i in range(P)):
+        raise PlanError(f"chunk ({q_begin}, {q_end}, {ctx_begin}) cannot be re-split into {P} parts")
+    return k
+
+
+def key_ranges(chunk: Chunk) -> List[Tuple[int, int]]:
+    """The key ranges whose partials a chunk merges: one range, two (split at
+    kv_split > 0) or P FLOPs-balanced parts (kv_split = -P)."""
+    qb, qe, cb, m = chunk
+    if m == 0:
+        return [(cb, qe)]
+    if m > 0:
+        return [(cb, m), (m, qe)]
+    k = resplit_boundaries(qb, qe, cb, -m)
+    return [(k[i], k[i + 1]) for i in range(len(k) - 1)]
+
+
+def plan_multiplex(L: int, N: int, PP: int) -> List[Chunk]:
+    """FLOPS chunks of one sequence with the edge chunks re-split as in SPPO
+    Table 3: chunk i and chunk N-1-i get PP - i parts (the largest count from
+    2 up to that which the chunk can hold; none below 2)."""
+    if PP < 1:
+        raise PlanError("PP must be positive")
+    b = boundaries(L, N, FLOPS)
+    chunks = [[b[i], b[i + 1], 0, 0] for i in range(N)]
+    for i in range(N):
+        want = PP - min(i, N - 1 - i)
+        for P in range(want, 1, -1):
+            try:
+                resplit_boundaries(b[i], b[i + 1], 0, P)
+            except PlanError:
+                continue
+            chunks[i][3] = -P
+            break
     return [tuple(c) for c in chunks]
 
 

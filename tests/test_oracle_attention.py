@@ -333,3 +333,18 @@ def test_grouped_backward_matches_autograd(G, cu):
         np.testing.assert_allclose(Qs[g].grad.numpy(), dqs[g], atol=1e-11)
     np.testing.assert_allclose(K.grad.numpy(), dk, atol=1e-11)
     np.testing.assert_allclose(V.grad.numpy(), dv, atol=1e-11)
+
+
+def test_chunked_forward_with_p_part_resplits():
+    """Chunks re-split into P parts of equal pair count (kv_split = -P) merge
+    back to the plain definition."""
+    T, D, sc = 1500, 8, 0.3
+    q, k, v = rand((T, D), 71), rand((T, D), 72), rand((T, D), 73)
+    O, L = A.forward(q, k, v, sc)
+    chunks = [(0, 700, 0, -4), (700, 1100, 0, -3), (1100, 1500, 0, -2)]
+    Oc, Lc = A.chunked_forward(q, k, v, chunks, sc)
+    np.testing.assert_allclose(Oc, O, atol=1e-12)
+    np.testing.assert_allclose(Lc, L, atol=1e-12)
+    for ch in P.plan_multiplex(T, 3, 3):
+        Op, Lp = A.chunked_forward(q, k, v, [ch], sc)
+        np.testing.assert_allclose(Op[ch[0]:ch[1]], O[ch[0]:ch[1]], atol=1e-12)

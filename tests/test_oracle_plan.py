@@ -6,6 +6,7 @@ roots), against the FLOP-balance bound that rounding to 128 allows, and against
 the stored expected plans in tests/golden/plans.json.
 """
 import json
+from decimal import Decimal, ROUND_FLOOR, localcontext
 import math
 import os
 import random
@@ -148,3 +149,90 @@ def test_golden_plans():
         else:
             got = P.plan(g["L"], g["N"], g["mode"])
         assert [list(c) for c in got] == g["chunks"], name
+
+
+# ---------------------------------------------------- re-split into P parts
+
+def test_key_pairs_closed_form_matches_counting():
+    rng = random.Random(3)
+    for _ in range(300):
+        cb = rng.randint(0, 300)
+        qb = cb + rng.randint(0, 300)
+        qe = qb + rng.randint(1, 300)
+        K = rng.randint(cb, qe)
+        brute = sum(1 for j in range(cb, K) for t in range(qb, qe) if j <= t)
+        assert P.key_pairs_before(qb, qe, cb, K) == brute
+
+
+def test_resplit_context_dominated_chunk_by_hand():
+    """Chunk (4096, 4224) with context from 0: every context key is seen by all
+    128 queries, the chunk's own keys by 128..1 of them. W = 4096*128 + 8256 =
+    532544; the quarter points fall at keys 1040.1, 2080.3, 3120.4 (inside the
+    uniform context), nearest multiples of 128: 1024, 2048, 3072."""
+    assert P.key_pairs_before(4096, 4224, 0, 4224) == 532544
+    assert P.resplit_boundaries(4096, 4224, 0, 4) == [0, 1024, 2048, 3072, 4224]
+
+
+@pytest.mark.parametrize("L,Pn", [(32768, 2), (32768, 4), (131072, 3), (4096, 5), (20000, 2)])
+def test_resplit_causal_chunk_closed_form(L, Pn):
+    """A chunk with no context: key j is seen by L - j queries, so the keys
+    before K carry K*L - K(K-1)/2 pairs and the equal-pair points are close to
+    L*(1 - sqrt(1 - p/P)) (50-digit decimals); the rule lands on the multiple
+    of 128 nearest to that, within one step when the point is near a half."""
+    k = P.resplit_boundaries(0, L, 0, Pn)
+    assert k[0] == 0 and k[-1] == L and len(k) == Pn + 1
+    with localcontext() as ctx:
+        ctx.prec = 50
+        for p in range(1, Pn):
+            x = Decimal(L) * (1 - (1 - Decimal(p) / Decimal(Pn)).sqrt())
+            near = 128 * int((x / 128 + Decimal("0.5")).to_integral_value(rounding=ROUND_FLOOR))
+            assert abs(k[p] - near) <= 128 and (k[p] == near or abs(x / 128 - int(x / 128) - Decimal("0.5")) < Decimal("0.01"))
+
+
+def test_resplit_parts_balanced():
+    rng = random.Random(9)
+    for _ in range(200):
+        cb = rng.randint(0, 5000)
+        qb = cb + rng.randint(0, 20000)
+        qe = qb + rng.randint(128, 20000)
+        Pn = rng.randint(2, 6)
+        try:
+            k = P.resplit_boundaries(qb, qe, cb, Pn)
+        except P.PlanError:
+            continue
+        W = P.key_pairs_before(qb, qe, cb, qe)
+        n = qe - qb
+        for p in range(Pn):
+            part = P.key_pairs_before(qb, qe, cb, k[p + 1]) - P.key_pairs_before(qb, qe, cb, k[p])
+            assert abs(part - W / Pn) <= 2 * 64 * n + n, (qb, qe, cb, Pn, p)
+
+
+def test_resplit_errors_and_key_ranges():
+    with pytest.raises(P.PlanError):
+        P.resplit_boundaries(0, 200, 0, 4)          # too few 128-token steps
+    with pytest.raises(P.PlanError):
+        P.resplit_boundaries(0, 4096, 0, 1)
+    assert P.key_ranges((0, 1000, 0, 0)) == [(0, 1000)]
+    assert P.key_ranges((0, 1000, 0, 300)) == [(0, 300), (300, 1000)]
+    k = P.resplit_boundaries(1000, 3000, 0, 3)
+    assert P.key_ranges((1000, 3000, 0, -3)) == [(k[0], k[1]), (k[1], k[2]), (k[2], k[3])]
+
+
+def test_plan_multiplex():
+    """SPPO Table 3 with PP = 4 and N = 8: chunks 0 and 7 in four parts, 1 and 6
+    in three, 2 and 5 in two, the middle ones whole."""
+    c = P.plan_multiplex(131072, 8, 4)
+    assert [x[3] for x in c] == [-4, -3, -2, 0, 0, -2, -3, -4]
+    assert [x[:2] for x in c] == [(b0, b1) for b0, b1 in zip(P.boundaries(131072, 8, P.FLOPS),
+                                                                P.boundaries(131072, 8, P.FLOPS)[1:])]
+    assert [x[3] for x in P.plan_multiplex(131072, 8, 1)] == [0] * 8
+    assert [x[3] for x in P.plan_multiplex(131072, 3, 3)] == [-3, -2, -3]
+    # L = 1024, N = 4, PP = 4, worked by hand. Chunk 0 = (0, 512) has no context:
+    # its equal-pair points for 4 parts, 512(1 - sqrt(1 - p/4)) = 68.6, 150, 256,
+    # round to 128, 128, 256 and collapse; for 3 parts, 94 and 216 round to 128
+    # and 256, so chunk 0 gets -3. Chunk 3 = (896, 1024) sees 896 context keys
+    # (128 queries each) and its own 128 keys (128..1 queries): W = 122944, the
+    # quarter points fall at keys 240.1, 480.3, 720.4 -> 256, 512, 768: -4.
+    small = P.plan_multiplex(1024, 4, 4)
+    assert small[0][3] == -3 and P.resplit_boundaries(0, 512, 0, 3) == [0, 128, 256, 512]
+    assert small[3][3] == -4 and P.resplit_boundaries(896, 1024, 0, 4) == [0, 256, 512, 768, 1024]
