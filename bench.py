@@ -193,6 +193,8 @@ def workload_config(w, args):
            "l2": "inputs larger than L2 (1 GiB per tensor); no flush", "parallelism": f"replicas x{args.gpus}"}
     if w.Hkv is not None:
         cfg["Hkv"] = w.Hkv
+    if args.plan != "default" and not w.packed:
+        cfg["plan_mode"] = args.plan
     return cfg
 
 
@@ -219,6 +221,8 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     if w.packed:
         chunks = cca.attn_plan_varlen(w.cu_seqlens(), w.max_chunk_tokens, w.mode)
+    elif args.plan.startswith("multiplex:"):
+        chunks = cca.attn_plan_multiplex(w.L, w.N, int(args.plan.split(":")[1]))
     else:
         chunks = cca.attn_plan(w.L, w.N, w.mode)
     q, k, v, do = workload_inputs(w, device=dev)
@@ -448,6 +452,8 @@ def main():
     ap.add_argument("--workload", default="7b_128k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan", default="default",
+                    help="default (the workload's plan) or multiplex:PP (SPPO Table 3 edge re-splits)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

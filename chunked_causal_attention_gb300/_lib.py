@@ -24,7 +24,7 @@ PLAN_FLOPS = 1
 PLAN_FLOPS_RESPLIT_EDGES = 2
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
+EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_plan_multiplex", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
            "attn_bwd_chunk", "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
 
@@ -65,6 +65,7 @@ _SP = ctypes.POINTER(attn_shape)
 _SIG = {
     "attn_plan": ([_I64, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
     "attn_plan_varlen": ([ctypes.POINTER(_I64), _I32, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "attn_plan_multiplex": ([_I64, _I32, _I32, _CP, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
     "attn_plan_infinipipe": ([ctypes.POINTER(_I64), _I32, _I32, _I64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                               _CP, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32), _I32, ctypes.POINTER(_I32)],
                              ctypes.c_int),
@@ -129,6 +130,14 @@ def attn_plan(L: int, N: int, mode: int) -> List[Tuple[int, int, int, int]]:
     out = (attn_chunk * max(1, N))()
     n = _I32(0)
     _check("attn_plan", lib().attn_plan(L, N, mode, out, N, ctypes.byref(n)))
+    return [(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[:n.value]]
+
+
+def attn_plan_multiplex(L: int, N: int, PP: int) -> List[Tuple[int, int, int, int]]:
+    """FLOPS chunks with SPPO Table 3 edge re-splits for PP stages (kv_split = -P)."""
+    out = (attn_chunk * max(1, N))()
+    n = _I32(0)
+    _check("attn_plan_multiplex", lib().attn_plan_multiplex(L, N, PP, out, N, ctypes.byref(n)))
     return [(c.q_begin, c.q_end, c.ctx_begin, c.kv_split) for c in out[:n.value]]
 
 

@@ -43,15 +43,31 @@ int check_shape(const attn_shape* s, Geom* g) {
     return ATTN_OK;
 }
 
+// Key-range boundaries of a chunk: [ctx, qe] unsplit, [ctx, m, qe] for a
+// split point m > 0, the P-part equal-pair boundaries for kv_split = -P.
+// False if the split is not valid for the chunk.
+bool key_bounds(const attn_chunk& x, std::vector<int32_t>& k) {
+    if (x.kv_split == 0) {
+        k = {x.ctx_begin, x.q_end};
+        return true;
+    }
+    if (x.kv_split > 0) {
+        k = {x.ctx_begin, x.kv_split, x.q_end};
+        return x.ctx_begin < x.kv_split && x.kv_split < x.q_end;
+    }
+    return x.kv_split >= -64 && resplit_bounds(x.q_begin, x.q_end, x.ctx_begin, -x.kv_split, k);
+}
+
 // Forward chunk rules: sorted by q_begin, disjoint, 0 <= ctx <= qb < qe <= T,
-// kv_split == 0 or ctx < m < qe.
+// kv_split == 0, ctx < m < qe, or -P (2 <= P <= 64) with valid boundaries.
 int check_chunks_fwd(const attn_chunk* c, int32_t n, int32_t T) {
     if (n < 0 || (n > 0 && !c)) return ATTN_E_INVAL;
+    std::vector<int32_t> k;
     for (int32_t i = 0; i < n; ++i) {
         const attn_chunk& x = c[i];
         if (!(0 <= x.ctx_begin && x.ctx_begin <= x.q_begin && x.q_begin < x.q_end && x.q_end <= T))
             return ATTN_E_INVAL;
-        if (x.kv_split != 0 && !(x.ctx_begin < x.kv_split && x.kv_split < x.q_end)) return ATTN_E_INVAL;
+        if (!key_bounds(x, k)) return ATTN_E_INVAL;
         if (i > 0 && c[i - 1].q_end > x.q_begin) return ATTN_E_INVAL;
     }
     return ATTN_OK;
@@ -77,7 +93,8 @@ int check_chunks_bwd(const attn_chunk* c, int32_t n, int32_t T) {
 struct FwdLayout {
     std::vector<FwdItem> items;
     std::vector<MergeSeg> segs;
-    size_t off_items, off_segs, off_parts, bytes;
+    std::vector<int32_t> kbounds;   // key-range boundaries of the segments
+    size_t off_items, off_segs, off_kb, off_parts, bytes;
     int64_t merge_work;
 };
 
@@ -85,34 +102,39 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
     const int64_t BH = (int64_t)g.B * g.H;
     L.items.clear();
     L.segs.clear();
+    L.kbounds.clear();
     int64_t part_floats = 0;   // running float offset inside the partial region
     L.merge_work = 0;
-    struct Pending { size_t seg; };
+    std::vector<int32_t> k;
     for (int32_t ci = 0; ci < n; ++ci) {
         const attn_chunk& x = c[ci];
-        const int32_t qb = x.q_begin, qe = x.q_end, cb = x.ctx_begin, m = x.kv_split;
-        int32_t pr0 = qe;  // first row that needs partials
-        int64_t off_a = -1, off_b = -1;
-        int32_t R = 0;
-        if (m) {
-            pr0 = m > qb ? qb + kTile * ((m - qb) / kTile) : qb;
-            R = qe - pr0;
-            int64_t blk = (int64_t)round_up((size_t)(BH * R * g.D + BH * R), 64);
-            off_a = part_floats;
-            off_b = part_floats + blk;
-            part_floats += 2 * blk;
+        const int32_t qb = x.q_begin, qe = x.q_end, cb = x.ctx_begin;
+        key_bounds(x, k);                       // validated by check_chunks_fwd
+        const int32_t P = (int32_t)k.size() - 1;
+        // rows before k_1 see only the first key range: whole 128-row tiles of
+        // them get their final result directly; partials start at the tile of k_1
+        const int32_t pr0 = P > 1 ? (k[1] > qb ? qb + kTile * ((k[1] - qb) / kTile) : qb) : qe;
+        const int32_t R = qe - pr0;
+        int64_t off0 = -1, blk = 0;
+        if (P > 1) {
+            blk = (int64_t)round_up((size_t)(BH * R * g.D + BH * R), 64);
+            off0 = part_floats;
+            part_floats += P * blk;
             MergeSeg s;
-            s.row0 = pr0; s.R = R; s.off_a = off_a; s.off_b = off_b; s.work0 = L.merge_work;
+            s.row0 = pr0; s.R = R; s.P = P; s.kb = (int32_t)L.kbounds.size();
+            s.off0 = off0; s.blk = blk; s.work0 = L.merge_work;
             L.merge_work += (int64_t)R * BH;
             L.segs.push_back(s);
+            L.kbounds.insert(L.kbounds.end(), k.begin(), k.end());
         }
         for (int32_t r0 = qb; r0 < qe; r0 += kTile) {
             int32_t r1 = std::min(r0 + kTile, qe);
-            if (!m || r1 <= m || r0 < pr0) {
+            if (P == 1 || r0 < pr0) {
                 L.items.push_back(FwdItem{r0, r1, cb, r1, -1, 0, 0});
             } else {
-                L.items.push_back(FwdItem{r0, r1, cb, std::min(m, r1), off_a, pr0, R});
-                L.items.push_back(FwdItem{r0, r1, m, r1, off_b, pr0, R});
+                // one partial per key range that some row of the tile can see
+                for (int32_t p = 0; p < P && k[p] < r1; ++p)
+                    L.items.push_back(FwdItem{r0, r1, k[p], std::min(k[p + 1], r1), off0 + p * blk, pr0, R});
             }
         }
     }
@@ -122,7 +144,8 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
     });
     L.off_items = kHeaderBytes;
     L.off_segs = L.off_items + round_up(L.items.size() * sizeof(FwdItem), kAlign);
-    L.off_parts = L.off_segs + round_up(L.segs.size() * sizeof(MergeSeg), kAlign);
+    L.off_kb = L.off_segs + round_up(L.segs.size() * sizeof(MergeSeg), kAlign);
+    L.off_parts = L.off_kb + round_up(L.kbounds.size() * sizeof(int32_t), kAlign);
     L.bytes = L.off_parts + round_up((size_t)part_floats * sizeof(float), kAlign);
 }
 
@@ -268,9 +291,11 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
     }
     if (do_merge && !L.segs.empty()) {
         if ((st = upload(w + L.off_segs, L.segs.data(), L.segs.size() * sizeof(MergeSeg), s))) return st;
+        if ((st = upload(w + L.off_kb, L.kbounds.data(), L.kbounds.size() * sizeof(int32_t), s))) return st;
         MergeArgs a;
         a.o = o; a.lse = lse; a.ws_f = ws_f;
         a.segs = (const MergeSeg*)(w + L.off_segs);
+        a.kbounds = (const int32_t*)(w + L.off_kb);
         a.n_segs = (int32_t)L.segs.size();
         a.total_work = L.merge_work;
         a.g = g;

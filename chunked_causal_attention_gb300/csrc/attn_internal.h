@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -32,14 +33,17 @@ struct FwdItem {
 };
 static_assert(sizeof(FwdItem) == 32, "FwdItem layout");
 
-// Merge segment of one re-split chunk: rows [row0, row0 + R), partial
-// blocks A and B at float offsets off_a, off_b (layout as FwdItem).
+// Merge segment of one re-split chunk: rows [row0, row0 + R), P partial
+// blocks, part p at float offset off0 + p * blk (layout as FwdItem); the
+// part's key range starts at kbounds[kb + p], and row t merges the parts
+// that start at or before t.
 struct MergeSeg {
     int32_t row0, R;
-    int64_t off_a, off_b;
+    int32_t P, kb;
+    int64_t off0, blk;
     int64_t work0;        // first work index of this segment (rows * BH prefix)
 };
-static_assert(sizeof(MergeSeg) == 32, "MergeSeg layout");
+static_assert(sizeof(MergeSeg) == 40, "MergeSeg layout");
 
 // One backward work item: keys [j0, j1) (j1 - j0 <= 128) of a document;
 // the queries [q_lo, q_end) are walked in blocks of 128 rows starting at
@@ -99,6 +103,7 @@ struct MergeArgs {
     void* o; float* lse;
     const float* ws_f;
     const MergeSeg* segs;
+    const int32_t* kbounds;   // key-range boundaries of all segments
     int32_t n_segs;
     int64_t total_work;   // sum over segments of R * B * H
     Geom g;
@@ -159,6 +164,10 @@ bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
 // (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
 bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);
 int device_sm_count();
+
+// Key-range boundaries cb = k_0 < ... < k_P = qe of a chunk re-split into P
+// parts of equal visible-pair count (kv_split = -P). False if they collapse.
+bool resplit_bounds(int32_t qb, int32_t qe, int32_t cb, int32_t P, std::vector<int32_t>& k);
 
 // Kernel launchers (return the launch error).
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s);   // fwd_tc.cu

@@ -12,7 +12,7 @@
 #include <cmath>
 #include <vector>
 
-#include "attn.h"
+#include "attn_internal.h"
 
 namespace {
 
@@ -304,4 +304,74 @@ extern "C" int attn_plan_infinipipe(const int64_t* seq_lens, int32_t nseq, int32
     *n_out = pos;
     *n_calls = (int32_t)calls.size();
     return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Re-split of a chunk's key range [cb, qe) into P parts with equal numbers of
+// visible (query, key) pairs of its queries [qb, qe) (SPPO §4 multiplexing,
+// read as a key/value split; Table 3 for the number of parts). The keys before
+// K carry pairs(K) = A*n + B*n - B(B-1)/2 with n = qe - qb, A = min(K, qb) - cb
+// context keys (seen by every query) and B = max(0, K - qb) of the chunk's own
+// keys (key j seen by the queries t >= j). Boundary k_p is cb + 128 m with m
+// the number of half-steps cb + 128 j - 64 (j >= 1, not past qe) where
+// P * pairs <= p * pairs(qe): the multiple of 128 nearest to the equal-pair
+// point, ties up. 128-bit integers throughout.
+namespace {
+
+using i128 = __int128;
+
+i128 key_pairs_before(int64_t qb, int64_t qe, int64_t cb, int64_t K) {
+    const i128 n = qe - qb;
+    const i128 A = std::min(K, qb) - cb;
+    const i128 B = std::max<int64_t>(0, K - qb);
+    return A * n + B * n - B * (B - 1) / 2;
+}
+
+}  // namespace
+
+namespace attn {
+
+bool resplit_bounds(int32_t qb, int32_t qe, int32_t cb, int32_t P, std::vector<int32_t>& k) {
+    if (P < 2 || P > 64 || !(cb <= qb && qb < qe)) return false;
+    const i128 W = key_pairs_before(qb, qe, cb, qe);
+    k.assign(P + 1, cb);
+    for (int32_t p = 1; p < P; ++p) {
+        // the test is monotone in m: bisection finds what a scan from m = 0 finds
+        int64_t lo = 0, hi = ((int64_t)qe - cb + 64) / 128 + 1;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) / 2;
+            const int64_t half = (int64_t)cb + 128 * mid - 64;
+            if (half <= qe && (i128)P * key_pairs_before(qb, qe, cb, half) <= (i128)p * W)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        k[p] = (int32_t)(cb + 128 * lo);
+    }
+    k[P] = qe;
+    for (int32_t i = 0; i < P; ++i)
+        if (!(k[i] < k[i + 1])) return false;
+    return true;
+}
+
+}  // namespace attn
+
+extern "C" int attn_plan_multiplex(int64_t L, int32_t N, int32_t PP, attn_chunk* out, int32_t cap,
+                                   int32_t* n_out) {
+    if (!n_out || (!out && cap > 0) || cap < 0) return ATTN_E_INVAL;
+    if (L <= 0 || L > INT32_MAX || N <= 0 || PP <= 0) return ATTN_E_INVAL;
+    std::vector<int64_t> b;
+    if (!boundaries(L, N, ATTN_PLAN_FLOPS, b)) return ATTN_E_INVAL;
+    std::vector<attn_chunk> c(N);
+    std::vector<int32_t> k;
+    for (int32_t i = 0; i < N; ++i) {
+        c[i] = attn_chunk{(int32_t)b[i], (int32_t)b[i + 1], 0, 0};
+        const int32_t want = PP - std::min(i, N - 1 - i);
+        for (int32_t P = std::min(want, 64); P >= 2; --P)
+            if (attn::resplit_bounds(c[i].q_begin, c[i].q_end, 0, P, k)) {
+                c[i].kv_split = -P;
+                break;
+            }
+    }
+    return emit(c, out, cap, n_out);
 }

@@ -1,18 +1,20 @@
-// Log-sum-exp merge of the two key-range partials of re-split chunks.
+// Log-sum-exp merge of the key-range partials of re-split chunks.
 //
-// SPPO §4 re-splits the subsequences next to the pipeline bubbles into two
-// sub-subsequences whose results are combined afterwards; the Ring
-// Self-Attention accumulation O = sum_i S_i V_i over key/value blocks is made
-// exact across blocks by the log-sum-exp rule:
-//     LSE = ln(e^{LSE_A} + e^{LSE_B}),  O = e^{LSE_A - LSE} O_A + e^{LSE_B - LSE} O_B,
-// where a part with no visible key (LSE = -inf) has weight 0.
+// SPPO §4 re-splits the subsequences next to the pipeline bubbles into
+// sub-subsequences whose results are combined afterwards (Table 3: as many as
+// there are idle devices); the Ring Self-Attention accumulation
+// O = sum_i S_i V_i over key/value blocks is made exact across blocks by the
+// log-sum-exp rule:
+//     LSE = ln sum_p e^{LSE_p},  O = sum_p e^{LSE_p - LSE} O_p,
+// where a part with no visible key (LSE = -inf, or a part that starts after
+// the row) has weight 0.
 // One warp per (segment row, batch*head); fp32 partials in, bf16 O and fp32 LSE out.
 #include "device_common.cuh"
 
 namespace attn {
 namespace {
 
-// One warp per (segment row, batch*head): merge the two partials.
+// One warp per (segment row, batch*head): merge the row's partials.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
     constexpr int PER = D / 32;   // floats per lane
@@ -28,25 +30,33 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
     const int i = (int)(local % sg.R);
     const int t = sg.row0 + i;
     const int64_t R = sg.R;
-    const float* A = a.ws_f + sg.off_a;
-    const float* Bp = a.ws_f + sg.off_b;
-    const float la = A[(int64_t)BH * R * D + (int64_t)bh * R + i];
-    const float lb = Bp[(int64_t)BH * R * D + (int64_t)bh * R + i];
-    const float mx = fmaxf(la, lb);
-    float wa = 0.f, wb = 0.f, lse = -INFINITY;
-    if (mx != -INFINITY) {
-        float ea = la == -INFINITY ? 0.f : __expf(la - mx);
-        float eb = lb == -INFINITY ? 0.f : __expf(lb - mx);
-        float tot = ea + eb;
-        lse = mx + __logf(tot);
-        wa = ea / tot;
-        wb = eb / tot;
-    }
-    const float* oa = A + ((int64_t)bh * R + i) * D + lane * PER;
-    const float* ob = Bp + ((int64_t)bh * R + i) * D + lane * PER;
+    const int32_t* kb = a.kbounds + sg.kb;
+    // parts whose key range starts at or before this row
+    int np = 0;
+    while (np < sg.P && kb[np] <= t) ++np;
+    float mx = -INFINITY;
+    for (int p = 0; p < np; ++p) mx = fmaxf(mx, a.ws_f[sg.off0 + p * sg.blk + (int64_t)BH * R * D + (int64_t)bh * R + i]);
     float r[PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) r[e] = wa * oa[e] + wb * ob[e];
+    for (int e = 0; e < PER; ++e) r[e] = 0.f;
+    float lse = -INFINITY;
+    if (mx != -INFINITY) {
+        float tot = 0.f;
+        for (int p = 0; p < np; ++p) {
+            const float* base = a.ws_f + sg.off0 + p * sg.blk;
+            const float lp = base[(int64_t)BH * R * D + (int64_t)bh * R + i];
+            if (lp == -INFINITY) continue;
+            const float ep = __expf(lp - mx);
+            tot += ep;
+            const float* op = base + ((int64_t)bh * R + i) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) r[e] = fmaf(ep, op[e], r[e]);
+        }
+        lse = mx + __logf(tot);
+        const float inv = 1.f / tot;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) r[e] *= inv;
+    }
     const int b = bh / a.g.H, h = bh % a.g.H;
     __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +
                        (int64_t)t * a.g.st + lane * PER;

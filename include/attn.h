@@ -74,10 +74,14 @@ extern "C" {
 
 /* One chunk (InfiniPipe §III-A1 split chunk {C, s}): query rows
  * [q_begin, q_end) with context C = q_begin - ctx_begin. ctx_begin is the
- * first visible key (the document start). kv_split = 0: no re-split; else m
- * with ctx_begin < m < q_end: the chunk's key range is cut into
- * [ctx_begin, m) and [m, q_end), each computed as a partial and merged by
- * log-sum-exp (SPPO §4 multiplexing, read as a key/value split). */
+ * first visible key (the document start). kv_split = 0: no re-split; m with
+ * ctx_begin < m < q_end: the chunk's key range is cut into [ctx_begin, m) and
+ * [m, q_end); -P (2 <= P <= 64): the key range is cut into P parts carrying
+ * equal numbers of visible (query, key) pairs of the chunk's queries, at the
+ * multiples of 128 from ctx_begin nearest to the equal-pair points (ties up;
+ * an error if they collapse). Each part is computed as a partial and the
+ * parts are merged by log-sum-exp (SPPO §4 multiplexing, read as a key/value
+ * split). */
 typedef struct {
     int32_t q_begin, q_end;
     int32_t ctx_begin;
@@ -106,6 +110,16 @@ typedef struct {
  * increasing), ATTN_E_CAPACITY (cap < N). */
 int attn_plan(int64_t L, int32_t N, int32_t mode,
               attn_chunk* out, int32_t cap, int32_t* n_out);
+
+/* FLOPS chunks of one sequence (as attn_plan) with the edge chunks re-split
+ * as in SPPO's multiplexed sequence partition (§4, Table 3) for PP pipeline
+ * stages: the SP range of an edge subsequence shrinks by one device per
+ * subsequence away from each pipeline end, so chunk i and chunk N-1-i get
+ * kv_split = -P with P the largest count from 2 up to PP - i that the chunk
+ * can hold (none when PP - i < 2). Errors as attn_plan (PP <= 0 is
+ * ATTN_E_INVAL). */
+int attn_plan_multiplex(int64_t L, int32_t N, int32_t PP,
+                        attn_chunk* out, int32_t cap, int32_t* n_out);
 
 /* Chunks of a packed batch (InfiniPipe §II-B, §III-A1). cu_seqlens: host
  * array of ndocs+1 non-decreasing offsets, cu_seqlens[0] = 0. A document of

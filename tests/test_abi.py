@@ -264,3 +264,32 @@ def test_plan_infinipipe_errors():
     assert L.attn_plan_infinipipe(lens, 3, 2, 10000, 1.0, 0.0, 0.0, out, 1, ctypes.byref(n), off, 1,
                                   ctypes.byref(nc)) == 8
     assert n.value >= 3 and nc.value >= 2
+
+
+def test_plan_multiplex_matches_oracle_exactly():
+    for L in (1024, 4096, 32768, 131072, 1 << 20, 100000):
+        for N in (1, 2, 4, 8, 16):
+            for PP in (1, 2, 3, 4, 8):
+                try:
+                    want = P.plan_multiplex(L, N, PP)
+                except P.PlanError:
+                    with pytest.raises(cca.AttnError):
+                        cca.attn_plan_multiplex(L, N, PP)
+                    continue
+                assert cca.attn_plan_multiplex(L, N, PP) == want, (L, N, PP)
+
+
+def test_p_part_resplit_validation_and_workspace():
+    """kv_split = -P: accepted when the P equal-pair boundaries are strictly
+    increasing; the forward workspace grows by one partial block per part."""
+    s = shape()                                                 # B1 H2 T1024 D64
+    base = cca.attn_workspace_size(s, [(0, 1024, 0, 0)], 0)
+    w2 = cca.attn_workspace_size(s, [(0, 1024, 0, -2)], 0)
+    w4 = cca.attn_workspace_size(s, [(0, 1024, 0, -4)], 0)
+    assert base < w2 < w4
+    for bad in ([(0, 200, 0, -4)], [(0, 1024, 0, -1)], [(0, 1024, 0, -65)]):
+        with pytest.raises(cca.AttnError) as e:
+            cca.attn_workspace_size(s, bad, 0)
+        assert e.value.status == 1
+    # the backward ignores kv_split but validates it like the forward
+    assert cca.attn_workspace_size(s, [(0, 1024, 0, -4)], 1) > 0

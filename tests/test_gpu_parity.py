@@ -189,3 +189,30 @@ def test_repeated_runs_bit_identical():
             continue
         assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
         assert torch.equal(dk, ref[2]) and torch.equal(dv, ref[3])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_p_part_resplits(D):
+    """Key ranges re-split into P parts of equal pair count (kv_split = -P),
+    including chunks with a long context and chunks whose parts end off the
+    128-row grid of the queries; every row against the oracle."""
+    L, H = 2300, 2
+    chunks = [(0, 640, 0, -3), (640, 1000, 0, -3), (1000, 1100, 0, -5), (1100, 2300, 0, -2)]
+    assert all(P.key_ranges(c) for c in chunks)
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=77 + D))
+    full_check(q, k, v, do, chunks, False, what=f"P-part D{D}")
+
+
+def test_p_part_resplits_packed_and_multiplex_plan():
+    lens = [2000, 1, 900, 1500]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    chunks = [(0, 1000, 0, -3), (1000, 2000, 0, -4), (2000, 2001, 2000, 0), (2001, 2901, 2001, -2),
+              (2901, 4401, 2901, -6)]
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 3, cu[-1], 128, seed=78, packed=True))
+    full_check(q, k, v, do, chunks, True, what="P-part packed")
+    plan = cca.attn_plan_multiplex(3000, 6, 4)
+    assert plan == P.plan_multiplex(3000, 6, 4) and plan[0][3] < 0
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, 3000, 128, seed=79))
+    full_check(q, k, v, do, plan, False, what="multiplex plan")

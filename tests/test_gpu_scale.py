@@ -123,3 +123,22 @@ def test_periodic_keys_every_row_and_key(name):
         check_grad(gdv, rdv, f"{name} periodic dV h{h} all keys")
         check_grad(gdv[:4096], rdv[:4096], f"{name} periodic dV h{h} first 4096 keys")
         check_grad(gdv[-4096:], rdv[-4096:], f"{name} periodic dV h{h} last 4096 keys")
+
+
+def test_7b_128k_multiplex_plan():
+    """The 128K workload with SPPO Table 3 edge re-splits for 4 pipeline
+    stages (chunks 0 and 15 in four key parts, 1 and 14 in three, 2 and 13 in
+    two): sampled rows and rows around every part boundary of the first chunk."""
+    w = WORKLOADS["7b_128k"]
+    q, k, v, do = (x.cuda() for x in workload_inputs(w))
+    chunks = cca.attn_plan_multiplex(w.L, w.N, 4)
+    assert chunks == P.plan_multiplex(w.L, w.N, 4)
+    assert [c[3] for c in chunks[:3]] == [-4, -3, -2] and [c[3] for c in chunks[-3:]] == [-2, -3, -4]
+    o, lse = cca.forward(q, k, v, chunks)
+    torch.cuda.synchronize()
+    sampled_rows_check(w, q, k, v, do, o, lse, None, 2048, 13, "128k multiplex", backward=False)
+    kb = P.resplit_boundaries(chunks[0][0], chunks[0][1], 0, 4)
+    r = np.array(sorted({x + d for x in kb[1:-1] for d in (-1, 0, 1)}))
+    qh, kh, vh = (head(x, 0, 9, False) for x in (q, k, v))
+    ro, rl = A.forward_rows(qh, kh, vh, r, w.scale)
+    check_fwd(head(o, 0, 9, False)[r], lse_head(lse, 0, 9)[r], ro, rl, "128k multiplex boundaries")
