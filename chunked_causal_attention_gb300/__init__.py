@@ -40,11 +40,19 @@ def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", pe
     return ws
 
 
+def _like(x):
+    """An uninitialised tensor with x's sizes and strides (so that one attn_shape
+    describes both), also when x is a view with gaps, such as the first D dims
+    of a wider buffer."""
+    import torch
+    return torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+
+
 def forward(q, k, v, chunks: Sequence, scale: Optional[float] = None, packed: bool = False, ws=None, stream=None):
     """(o, lse) of chunked causal attention; q, k, v bf16 [B, H, L, D] (or packed [T, H, D])."""
     import torch
     shape = shape_of(q, scale, packed, k)
-    o = torch.empty_like(q)
+    o = _like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(shape, chunks, 0, q.device)
@@ -57,7 +65,7 @@ def backward(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[float] = N
     """(dq, dk, dv) for upstream gradient dout, given the forward's o and lse."""
     import torch
     shape = shape_of(q, scale, packed, k)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = _like(q), _like(k), _like(v)
     if ws is None:
         ws = workspace(shape, chunks, 1, q.device)
     attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream)
@@ -71,7 +79,7 @@ def forward_streamed(q, k, v, chunks: Sequence, scale: Optional[float] = None, p
     are resident in k, v."""
     import torch
     shape = shape_of(q, scale, packed, k)
-    o = torch.empty_like(q)
+    o = _like(q)
     lse = torch.empty((shape.B, shape.H, shape.T), dtype=torch.float32, device=q.device)
     calls = [c if isinstance(c[0], (list, tuple)) else [c] for c in chunks]
     ws = workspace(shape, calls, PASS_FWD, q.device, per_chunk=True)
@@ -87,7 +95,7 @@ def backward_streamed(q, k, v, o, lse, dout, chunks: Sequence, scale: Optional[f
     the calls (attn_bwd_chunk). Returns (dq, dk, dv, dk_acc, dv_acc)."""
     import torch
     shape = shape_of(q, scale, packed, k)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = _like(q), _like(k), _like(v)
     # fp32 accumulators at the same element offsets as k and v
     dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=k.device).zero_()
     dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=v.device).zero_()

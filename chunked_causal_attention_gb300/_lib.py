@@ -15,6 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_OK = 0
+ATTN_E_INVAL = 1
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_E_INVAL", 2: "ATTN_E_ALIGN", 3: "ATTN_E_UNSUPPORTED",
                 4: "ATTN_E_WORKSPACE", 5: "ATTN_E_CUDA", 6: "ATTN_E_TIMEOUT", 7: "ATTN_E_BOUNDS",
                 8: "ATTN_E_CAPACITY"}
@@ -217,6 +218,47 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _layout_ok(t, B: int, H: int, T: int, D: int, sb: int, st: int, sh: int) -> bool:
+    """t addresses element (b, t, h, d) at b*sb + t*st + h*sh + d: a dense
+    [B, H, T, D] view, or a packed [T, H, D] one when B == 1 (strides of size-1
+    dims are free)."""
+    if t.dim() == 4:
+        want_size, want_stride = (B, H, T, D), (sb, sh, st, 1)
+    elif t.dim() == 3 and B == 1:
+        want_size, want_stride = (T, H, D), (st, sh, 1)
+    else:
+        return False
+    if tuple(t.shape) != want_size:
+        return False
+    return all(n == 1 or got == want for n, got, want in zip(want_size, t.stride(), want_stride))
+
+
+def _expect(fn: str, shape: attn_shape, kind: str, *tensors) -> None:
+    """The C ABI takes one set of strides per kind of tensor and raw pointers,
+    so it cannot see a tensor whose layout differs from the shape's; such a
+    tensor would be read or written at the shape's offsets. Every tensor
+    argument must therefore have the shape's sizes and strides: kind 'q'
+    (q, o, dout, dq: bf16, query strides), 'kv' (k, v, dk, dv: bf16,
+    key/value strides), 'acc' (fp32 dK/dV accumulators: key/value strides),
+    'lse' (fp32 [B, H, T] contiguous). None is passed through (the library
+    rejects null pointers itself). Raises AttnError(ATTN_E_INVAL)."""
+    import torch
+    grouped = kind in ("kv", "acc") and shape.Hkv > 0
+    H = shape.Hkv if grouped else shape.H
+    sb, st, sh = (shape.sb_kv, shape.st_kv, shape.sh_kv) if grouped else (shape.sb, shape.st, shape.sh)
+    for t in tensors:
+        if t is None:
+            continue
+        if kind == "lse":
+            ok = (t.dtype == torch.float32 and t.is_cuda and t.is_contiguous()
+                  and t.numel() == shape.B * shape.H * shape.T)
+        else:
+            dt = torch.float32 if kind == "acc" else torch.bfloat16
+            ok = t.dtype == dt and t.is_cuda and _layout_ok(t, shape.B, H, shape.T, shape.D, sb, st, sh)
+        if not ok:
+            raise AttnError(fn, ATTN_E_INVAL)
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -225,12 +267,18 @@ def _stream(stream) -> Optional[int]:
 
 
 def attn_fwd(q, k, v, chunks, shape, o, lse, ws, stream=None) -> None:
+    _expect("attn_fwd", shape, "q", q, o)
+    _expect("attn_fwd", shape, "kv", k, v)
+    _expect("attn_fwd", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape), _ptr(o), _ptr(lse),
                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def attn_fwd_tiles(q, k, v, chunks, shape, o, lse, ws, stream=None) -> None:
+    _expect("attn_fwd_tiles", shape, "q", q, o)
+    _expect("attn_fwd_tiles", shape, "kv", k, v)
+    _expect("attn_fwd_tiles", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_fwd_tiles", lib().attn_fwd_tiles(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape), _ptr(o),
                                                   _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
@@ -238,12 +286,17 @@ def attn_fwd_tiles(q, k, v, chunks, shape, o, lse, ws, stream=None) -> None:
 
 
 def attn_fwd_merge(chunks, shape, o, lse, ws, stream=None) -> None:
+    _expect("attn_fwd_merge", shape, "q", o)
+    _expect("attn_fwd_merge", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_fwd_merge", lib().attn_fwd_merge(arr, n, ctypes.byref(shape), _ptr(o), _ptr(lse), _ptr(ws),
                                                   ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream=None) -> None:
+    _expect("attn_bwd", shape, "q", q, o, dout, dq)
+    _expect("attn_bwd", shape, "kv", k, v, dk, dv)
+    _expect("attn_bwd", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_bwd", lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr, n,
                                       ctypes.byref(shape), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
@@ -251,12 +304,16 @@ def attn_bwd(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, ws, stream=None) 
 
 
 def attn_bwd_prep(o, dout, chunks, shape, ws, stream=None) -> None:
+    _expect("attn_bwd_prep", shape, "q", o, dout)
     arr, n = chunk_array(chunks)
     _check("attn_bwd_prep", lib().attn_bwd_prep(_ptr(o), _ptr(dout), arr, n, ctypes.byref(shape), _ptr(ws),
                                                 ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def attn_bwd_tiles(q, k, v, lse, dout, chunks, shape, dk, dv, ws, stream=None) -> None:
+    _expect("attn_bwd_tiles", shape, "q", q, dout)
+    _expect("attn_bwd_tiles", shape, "kv", k, v, dk, dv)
+    _expect("attn_bwd_tiles", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_bwd_tiles", lib().attn_bwd_tiles(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dout), arr, n,
                                                   ctypes.byref(shape), _ptr(dk), _ptr(dv), _ptr(ws),
@@ -264,6 +321,7 @@ def attn_bwd_tiles(q, k, v, lse, dout, chunks, shape, dk, dv, ws, stream=None) -
 
 
 def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
+    _expect("attn_bwd_dq", shape, "q", dq)
     arr, n = chunk_array(chunks)
     _check("attn_bwd_dq", lib().attn_bwd_dq(arr, n, ctypes.byref(shape), _ptr(dq), _ptr(ws),
                                             ws.numel() * ws.element_size(), _stream(stream)))
@@ -271,6 +329,10 @@ def attn_bwd_dq(chunks, shape, dq, ws, stream=None) -> None:
 
 def attn_bwd_chunk(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, dk_acc, dv_acc, ws, stream=None) -> None:
     """Backward of the rows of a set of chunks (chunk-streamed; see include/attn.h)."""
+    _expect("attn_bwd_chunk", shape, "q", q, o, dout, dq)
+    _expect("attn_bwd_chunk", shape, "kv", k, v, dk, dv)
+    _expect("attn_bwd_chunk", shape, "acc", dk_acc, dv_acc)
+    _expect("attn_bwd_chunk", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_bwd_chunk", lib().attn_bwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), arr, n,
                                                   ctypes.byref(shape), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dk_acc),
@@ -281,6 +343,9 @@ def attn_bwd_chunk(q, k, v, o, lse, dout, chunks, shape, dq, dk, dv, dk_acc, dv_
 def attn_fwd_noalloc(q, k, v, chunks, shape, o, lse, stream=None) -> None:
     """Forward without a workspace argument: for callers that cannot allocate
     device memory; uses the library's own scratch (see include/attn.h)."""
+    _expect("attn_fwd_noalloc", shape, "q", q, o)
+    _expect("attn_fwd_noalloc", shape, "kv", k, v)
+    _expect("attn_fwd_noalloc", shape, "lse", lse)
     arr, n = chunk_array(chunks)
     _check("attn_fwd_noalloc", lib().attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), arr, n, ctypes.byref(shape),
                                                       _ptr(o), _ptr(lse), _stream(stream)))

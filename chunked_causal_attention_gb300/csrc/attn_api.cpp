@@ -23,7 +23,7 @@ int check_shape(const attn_shape* s, Geom* g) {
     if (s->B <= 0 || s->H <= 0 || s->T <= 0 || s->D <= 0) return ATTN_E_INVAL;
     if (s->T > INT32_MAX || s->B > INT32_MAX || s->H > INT32_MAX) return ATTN_E_INVAL;
     if ((int64_t)s->B * s->H > (1ll << 24)) return ATTN_E_INVAL;
-    if (s->D != 64 && s->D != 128) return ATTN_E_UNSUPPORTED;
+    if (s->D < 8 || s->D > 128 || (s->D % 8)) return ATTN_E_UNSUPPORTED;
     if (s->sb <= 0 || s->st <= 0 || s->sh <= 0) return ATTN_E_INVAL;
     if (!std::isfinite(s->scale)) return ATTN_E_INVAL;
     if ((s->sb % 8) || (s->st % 8) || (s->sh % 8)) return ATTN_E_ALIGN;

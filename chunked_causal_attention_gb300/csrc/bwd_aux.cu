@@ -10,6 +10,11 @@
 namespace attn {
 namespace {
 
+// Two bf16 (low half first) to floats: a bf16 is the upper 16 bits of its float.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
 // Token of workspace row r: the segment with the largest ws_row0 <= r.
 __device__ __forceinline__ int token_of_row(const RowSeg* segs, int n, int r) {
     int lo = 0, hi = n - 1;
@@ -21,50 +26,47 @@ __device__ __forceinline__ int token_of_row(const RowSeg* segs, int n, int r) {
 }
 
 // One warp per (batch*head, token): delta = dO . O; zero the dQ accumulator row.
-template <int D>
+// Lane l takes the four elements from d = 4l (D is a multiple of 8, at most 128).
 __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
-    constexpr int PER = D / 32;
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
+    const int D = a.g.D;
     const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
     const int b = bh / a.g.H, h = bh % a.g.H;
-    const int64_t off = (int64_t)b * a.g.sb + (int64_t)h * a.g.sh + (int64_t)t * a.g.st + lane * PER;
-    const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o) + off;
-    const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout) + off;
+    const int64_t off = (int64_t)b * a.g.sb + (int64_t)h * a.g.sh + (int64_t)t * a.g.st;
+    const int d = 4 * lane;
     float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) {
-        __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(O + e);
-        __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(dO + e);
-        float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
-        acc = fmaf(fx.x, fy.x, acc);
-        acc = fmaf(fx.y, fy.y, acc);
+    if (d < D) {
+        const uint2 xo = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + off + d);
+        const uint2 xd = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.dout) + off + d);
+        const float2 o0 = bf16x2_to_float2(xo.x), o1 = bf16x2_to_float2(xo.y);
+        const float2 g0 = bf16x2_to_float2(xd.x), g1 = bf16x2_to_float2(xd.y);
+        acc = fmaf(o0.x, g0.x, fmaf(o0.y, g0.y, fmaf(o1.x, g1.x, o1.y * g1.y)));
+        *reinterpret_cast<float4*>(a.dq_acc + w * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (lane == 0) a.delta[w] = acc;
-    float* q = a.dq_acc + w * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) q[e] = 0.f;
 }
 
-// One warp per (batch*head, token): dq = bf16(accumulator).
-template <int D>
+// One warp per (batch*head, token): dq = bf16(accumulator); lane l takes the
+// four elements from d = 4l.
 __global__ void __launch_bounds__(256) dq_kernel(DqArgs a) {
-    constexpr int PER = D / 32;
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)a.g.B * a.g.H * a.rows;
     if (w >= total) return;
+    const int D = a.g.D;
+    const int d = 4 * lane;
+    if (d >= D) return;
     const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
     const int b = bh / a.g.H, h = bh % a.g.H;
-    const float* src = a.dq_acc + w * D + lane * PER;
+    const float4 v = *reinterpret_cast<const float4*>(a.dq_acc + w * D + d);
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +
-                         (int64_t)t * a.g.st + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(src[e], src[e + 1]);
+                         (int64_t)t * a.g.st + d;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
 }
 
 }  // namespace
@@ -73,10 +75,7 @@ cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
     const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.rows + 7) / 8;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    if (a.g.D == 128)
-        prep_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(a);
-    else
-        prep_kernel<64><<<(unsigned)blocks, 256, 0, s>>>(a);
+    prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -84,10 +83,7 @@ cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
     const int64_t blocks = ((int64_t)a.g.B * a.g.H * a.rows + 7) / 8;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    if (a.g.D == 128)
-        dq_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(a);
-    else
-        dq_kernel<64><<<(unsigned)blocks, 256, 0, s>>>(a);
+    dq_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -160,7 +160,10 @@ __device__ __forceinline__ void sg_block(uint32_t tm, int grp, int krow, int key
 // GROUPED: key/value heads shared by several query heads. The ungrouped
 // instantiation has G = 1 at compile time, which keeps the per-block walk of
 // the softmax-gradient warps as light as it was before grouping existed.
-template <int D, bool GROUPED>
+// PAD: the head dim is below the tile width D (its dims past it load as zeros
+// and are not written); the unpadded instantiations keep every write bound at
+// compile time.
+template <int D, bool GROUPED, bool PAD>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -405,6 +408,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             // bf16 only for the chunk's own keys (complete once their chunk has run)
             float* acc = a.dk_acc ? (grp == 0 ? a.dk_acc : a.dv_acc) + roff : nullptr;
             const bool emit = acc == nullptr || key >= item.emit_from;
+            const int Dv = PAD ? a.g.D : D;        // dims written (the tile's dims past the head dim are zero)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -418,6 +422,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                         float4* a4 = reinterpret_cast<float4*>(acc + c * 32);
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
+                            if (c * 32 + u * 4 >= Dv) break;
                             float4 x = a4[u];
                             x.x += f[4 * u]; x.y += f[4 * u + 1]; x.z += f[4 * u + 2]; x.w += f[4 * u + 3];
                             a4[u] = x;
@@ -428,6 +433,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
+                            if (c * 32 + u * 8 >= Dv) break;
                             uint4 v;
                             v.x = pack_bf16(f[8 * u + 0], f[8 * u + 1]);
                             v.y = pack_bf16(f[8 * u + 2], f[8 * u + 3]);
@@ -490,9 +496,12 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 named_sync(3, 128);
                 if (qrow == 0) {
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
+                    // 32-column boxes that start past the head dim hold only the zero
+                    // dims of the tile; a box that runs past it is clipped by the TMA unit
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc)
-                        tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 + item.row_off, bhq);
+                        if (!PAD || cc * 32 < a.g.D)
+                            tma_reduce_add_3d(&tmdq, st + cc * 16384, cc * 32, i0 + item.row_off, bhq);
                     bulk_commit();
                     bulk_wait_read_all();
                     mbar_arrive(bar(LY::B_QEMPTY + s));      // the producer may refill this stage
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     }
 }
 
-template <int D, bool GROUPED>
+template <int D, bool GROUPED, bool PAD>
 cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
@@ -538,18 +547,22 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     if (work > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = BwdTcLayout<D>::ALLOC;
     cudaError_t e =
-        cudaFuncSetAttribute(bwd_tc_kernel<D, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(bwd_tc_kernel<D, GROUPED, PAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_tc_kernel<D, GROUPED><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
+    bwd_tc_kernel<D, GROUPED, PAD><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s) {
-    if (a.g.Hkv != a.g.H) return a.g.D == 128 ? launch_d<128, true>(a, s) : launch_d<64, true>(a, s);
-    return a.g.D == 128 ? launch_d<128, false>(a, s) : launch_d<64, false>(a, s);
+    // head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles
+    const bool grouped = a.g.Hkv != a.g.H;
+    if (a.g.D == 128) return grouped ? launch_d<128, true, false>(a, s) : launch_d<128, false, false>(a, s);
+    if (a.g.D == 64) return grouped ? launch_d<64, true, false>(a, s) : launch_d<64, false, false>(a, s);
+    if (a.g.D > 64) return grouped ? launch_d<128, true, true>(a, s) : launch_d<128, false, true>(a, s);
+    return grouped ? launch_d<64, true, true>(a, s) : launch_d<64, false, true>(a, s);
 }
 
 }  // namespace attn

@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t oa = tmem + lane_addr + kColO;
             const int b_ = bh / a.g.H, h_ = bh % a.g.H;
             const bool live = t_row < item.r1;
+            const int Dv = a.g.D;                      // dims written: D (the tile's dims past it are zero)
             if (item.part_off < 0) {
                 __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b_ * a.g.sb +
                                      (int64_t)h_ * a.g.sh + (int64_t)t_row * a.g.st;
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
+                            if (c * 32 + i * 8 >= Dv) break;
                             uint4 v;
                             v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
                             v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             } else {
                 const int64_t R = item.part_R;
                 const int i_row = t_row - item.part_row0;
-                float* dst = a.ws_f + item.part_off + ((int64_t)bh * R + i_row) * D;
+                float* dst = a.ws_f + item.part_off + ((int64_t)bh * R + i_row) * Dv;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -368,11 +370,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                            if (c * 32 + i * 4 < Dv)
+                                d4[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                                    __uint_as_float(o[4 * i + 2]) * inv,
+                                                    __uint_as_float(o[4 * i + 3]) * inv);
                     }
                 }
-                if (live) a.ws_f[item.part_off + (int64_t)BH * R * D + (int64_t)bh * R + i_row] = lse;
+                if (live) a.ws_f[item.part_off + (int64_t)BH * R * Dv + (int64_t)bh * R + i_row] = lse;
             }
             tc_fence_before();
             mbar_arrive(bar(LY::B_OFREE));
@@ -421,7 +425,8 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s) {
-    return a.g.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+    // head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles
+    return a.g.D > 64 ? launch_d<128>(a, s) : launch_d<64>(a, s);
 }
 
 }  // namespace attn

@@ -14,13 +14,13 @@
 namespace attn {
 namespace {
 
-// One warp per (segment row, batch*head): merge the row's partials.
-template <int D>
+// One warp per (segment row, batch*head): merge the row's partials. Lane l
+// takes the four elements from d = 4l (D is a multiple of 8, at most 128).
 __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
-    constexpr int PER = D / 32;   // floats per lane
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= a.total_work) return;
+    const int D = a.g.D;
     int si = 0;
     while (si + 1 < a.n_segs && a.segs[si + 1].work0 <= w) ++si;
     const MergeSeg sg = a.segs[si];
@@ -36,9 +36,8 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
     while (np < sg.P && kb[np] <= t) ++np;
     float mx = -INFINITY;
     for (int p = 0; p < np; ++p) mx = fmaxf(mx, a.ws_f[sg.off0 + p * sg.blk + (int64_t)BH * R * D + (int64_t)bh * R + i]);
-    float r[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) r[e] = 0.f;
+    const int d = 4 * lane;
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse = -INFINITY;
     if (mx != -INFINITY) {
         float tot = 0.f;
@@ -48,20 +47,25 @@ __global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
             if (lp == -INFINITY) continue;
             const float ep = __expf(lp - mx);
             tot += ep;
-            const float* op = base + ((int64_t)bh * R + i) * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) r[e] = fmaf(ep, op[e], r[e]);
+            if (d < D) {
+                const float4 v = *reinterpret_cast<const float4*>(base + ((int64_t)bh * R + i) * D + d);
+                r.x = fmaf(ep, v.x, r.x);
+                r.y = fmaf(ep, v.y, r.y);
+                r.z = fmaf(ep, v.z, r.z);
+                r.w = fmaf(ep, v.w, r.w);
+            }
         }
         lse = mx + __logf(tot);
         const float inv = 1.f / tot;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) r[e] *= inv;
+        r.x *= inv;
+        r.y *= inv;
+        r.z *= inv;
+        r.w *= inv;
     }
     const int b = bh / a.g.H, h = bh % a.g.H;
     __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +
-                       (int64_t)t * a.g.st + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(O + e) = pack_bf16(r[e], r[e + 1]);
+                       (int64_t)t * a.g.st;
+    if (d < D) *reinterpret_cast<uint2*>(O + d) = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
     if (lane == 0) a.lse[(int64_t)bh * a.g.T + t] = lse;
 }
 
@@ -71,10 +75,7 @@ cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s) {
     if (a.total_work <= 0) return cudaSuccess;
     const int64_t blocks = (a.total_work + 7) / 8;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    if (a.g.D == 128)
-        merge_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(a);
-    else
-        merge_kernel<64><<<(unsigned)blocks, 256, 0, s>>>(a);
+    merge_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -94,9 +94,13 @@ def test_workspace_size_validation():
     ch = cca.attn_plan(1024, 4, 0)
     assert cca.attn_workspace_size(shape(), ch, 0) >= 256
     assert cca.attn_workspace_size(shape(), ch, 1) >= 2 * 1024 * 64 * 4
-    with pytest.raises(cca.AttnError) as e:
-        cca.attn_workspace_size(shape(D=96), ch, 0)
-    assert e.value.status == 3
+    # head dims: multiples of 8 from 8 to 128
+    for D in (8, 40, 80, 96, 120):
+        assert cca.attn_workspace_size(shape(D=D), ch, 1) >= 2 * 1024 * D * 4
+    for D in (4, 100, 136, 256):
+        with pytest.raises(cca.AttnError) as e:
+            cca.attn_workspace_size(shape(D=D), ch, 0)
+        assert e.value.status == 3
     bad = [(0, 600, 0, 0), (500, 1024, 0, 0)]                  # overlapping
     with pytest.raises(cca.AttnError):
         cca.attn_workspace_size(shape(), bad, 0)
@@ -147,9 +151,10 @@ def test_compute_calls_reject_bad_arguments_on_host():
     s = shape()
     fake = ctypes.c_void_p(4096)
     ws = ctypes.c_void_p(1 << 20)
-    # D unsupported
-    s96 = cca.make_shape(1, 2, 1024, 96, 2 * 1024 * 96, 96, 1024 * 96, 0.1)
-    assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(s96), fake, fake, ws, 1 << 30, None) == 3
+    # D unsupported (not a multiple of 8, or above 128)
+    for D in (100, 136):
+        sD = cca.make_shape(1, 2, 1024, D, 2 * 1024 * D, D, 1024 * D, 0.1)
+        assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(sD), fake, fake, ws, 1 << 30, None) == 3
     # misaligned q
     assert L.attn_fwd(ctypes.c_void_p(4098), fake, fake, ch, n, ctypes.byref(s), fake, fake, ws, 1 << 30, None) == 2
     # workspace too small / missing
@@ -293,3 +298,42 @@ def test_p_part_resplit_validation_and_workspace():
         assert e.value.status == 1
     # the backward ignores kv_split but validates it like the forward
     assert cca.attn_workspace_size(s, [(0, 1024, 0, -4)], 1) > 0
+
+
+def test_tensor_layout_check():
+    """The binding checks every tensor against the attn_shape before a call:
+    the C ABI takes one set of strides and raw pointers, so a tensor with
+    another layout would be read or written at the shape's offsets."""
+    import torch
+    from chunked_causal_attention_gb300._lib import _layout_ok
+    x = torch.zeros(2, 3, 50, 64)
+    s = cca.shape_of(x)
+    assert _layout_ok(x, s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+    tm = torch.zeros(2, 50, 3, 64).permute(0, 2, 1, 3)                 # token-major storage
+    s = cca.shape_of(tm)
+    assert _layout_ok(tm, s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+    assert not _layout_ok(x, s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)      # same sizes, other strides
+    wide = torch.zeros(2, 3, 50, 128)[..., :80]                          # first 80 dims of a wider buffer
+    s = cca.shape_of(wide)
+    assert (s.D, s.st) == (80, 128) and _layout_ok(wide, s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+    assert not _layout_ok(torch.zeros(2, 3, 50, 80), s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+    p = torch.zeros(70, 4, 32)                                           # packed [T, H, D]
+    s = cca.shape_of(p, packed=True)
+    assert _layout_ok(p, s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+    assert not _layout_ok(p[:69], s.B, s.H, s.T, s.D, s.sb, s.st, s.sh)
+
+
+def test_compute_wrappers_reject_cpu_and_mismatched_tensors():
+    """Rejected on the host with ATTN_E_INVAL before the library is called."""
+    import torch
+    q = torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16)
+    s = cca.shape_of(q)
+    ch = cca.attn_plan(256, 1, 0)
+    lse = torch.zeros(1, 2, 256)
+    ws = torch.zeros(1, dtype=torch.uint8)
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_fwd(q, q, q, ch, s, q, lse, ws)                        # host tensors
+    assert e.value.status == 1
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_bwd_chunk(q, q, q, q, lse, q, ch, s, q, q, q, q.float(), q.float(), ws)
+    assert e.value.status == 1

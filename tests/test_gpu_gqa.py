@@ -47,7 +47,7 @@ def grouped_check(q, k, v, do, o, lse, dq, dk, dv, cu, packed, what):
 
 
 @pytest.mark.parametrize("L", [129, 1000])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [48, 64, 96, 128])
 @pytest.mark.parametrize("H,Hkv", [(8, 2), (4, 1), (3, 3)])
 def test_grouped_dense(L, D, H, Hkv):
     chunks = P.plan(L, 1 if L < 300 else 3, P.FLOPS_RESPLIT_EDGES)

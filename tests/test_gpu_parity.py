@@ -191,7 +191,7 @@ def test_repeated_runs_bit_identical():
         assert torch.equal(dk, ref[2]) and torch.equal(dv, ref[3])
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 96, 128])
 def test_p_part_resplits(D):
     """Key ranges re-split into P parts of equal pair count (kv_split = -P),
     including chunks with a long context and chunks whose parts end off the
@@ -216,3 +216,43 @@ def test_p_part_resplits_packed_and_multiplex_plan():
     assert plan == P.plan_multiplex(3000, 6, 4) and plan[0][3] < 0
     q, k, v, do = (x.cuda() for x in make_inputs(1, 2, 3000, 128, seed=79))
     full_check(q, k, v, do, plan, False, what="multiplex plan")
+
+
+@pytest.mark.parametrize("D", [8, 40, 80, 96, 120])
+def test_head_dims_between_tile_widths(D):
+    """Head dims that are not 64 or 128 run on the 64- or 128-wide tiles with
+    the dims past D loaded as zeros: dense rows with ragged tiles and an edge
+    re-split (the merge path), then packed documents, every row against the
+    oracle."""
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 3, 1000, D, seed=90 + D))
+    full_check(q, k, v, do, P.plan(1000, 3, P.FLOPS_RESPLIT_EDGES), False, what=f"D{D} dense")
+    lens = [1, 127, 129, 300, 700]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, cu[-1], D, seed=95 + D, packed=True))
+    full_check(q, k, v, do, P.plan_varlen(cu, 256, P.FLOPS_RESPLIT_EDGES), True, what=f"D{D} packed")
+
+
+def test_head_dim_padding_leaves_neighbours_untouched():
+    """With D = 80 on the 128-wide tiles, the dims past D of a row are never
+    written: rows of a wider buffer viewed with D = 80 keep their tail."""
+    L, H, D, W = 700, 2, 80, 128
+    base = [x.cuda() for x in make_inputs(1, H, L, W, seed=97)]
+    views = [x[..., :D] for x in base]                               # strides of the W-wide buffer
+    chunks = P.plan(L, 2, P.FLOPS_RESPLIT_EDGES)
+    shape = cca.shape_of(views[0])
+    o_buf = torch.full((1, H, L, W), 5.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, H, L), dtype=torch.float32, device="cuda")
+    ws = cca.workspace(shape, chunks, 0)
+    cca.attn_fwd(*views[:3], chunks, shape, o_buf[..., :D], lse, ws)
+    grads = [torch.full((1, H, L, W), 3.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    wsb = cca.workspace(shape, chunks, 1)
+    cca.attn_bwd(*views[:3], o_buf[..., :D], lse, views[3], chunks, shape, *(g[..., :D] for g in grads), wsb)
+    torch.cuda.synchronize()
+    assert cca.attn_status(ws) == 0 and cca.attn_status(wsb) == 0
+    assert torch.all(o_buf[..., D:] == 5.0)
+    for g in grads:
+        assert torch.all(g[..., D:] == 3.0)
+    o, lse2, dq, dk, dv = full_check(*views, chunks, False, what="D80 in a 128-wide buffer")
+    assert torch.equal(o_buf[..., :D], o) and torch.equal(lse, lse2)

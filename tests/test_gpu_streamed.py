@@ -188,3 +188,12 @@ def test_infinipipe_plan_streamed():
         check_grad(head(dq, 0, h, True), rdq, f"infinipipe dQ h{h}")
         check_grad(head(dk, 0, h, True), rdk, f"infinipipe dK h{h}")
         check_grad(head(dv, 0, h, True), rdv, f"infinipipe dV h{h}")
+
+
+@pytest.mark.parametrize("D", [40, 96])
+def test_streamed_head_dims_between_tile_widths(D):
+    """Chunk-streamed calls with fp32 dK/dV accumulators of a head dim that
+    is neither 64 nor 128."""
+    chunks = P.plan(1000, 4, P.FLOPS_RESPLIT_EDGES)
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 2, 1000, D, seed=310 + D))
+    streamed_check(q, k, v, do, chunks, False, f"streamed D{D}")
