@@ -340,10 +340,11 @@ def run_ours(args):
     del dk_acc, dv_acc, ws_fc, ws_bc
 
     # End to end through the public API: every step uploads its inputs from pinned
-    # host memory and reads its results back. Copies run on their own stream with
-    # two sets of device buffers, so step i+1's upload and step i-1's read-back
-    # overlap step i's kernels; each step still moves all of its own bytes.
-    e2e_steps = max(4, min(args.steps, 6))    # enough steps that the pipeline's fill and drain stay small
+    # host memory and reads its results back. Uploads and read-backs run on two
+    # copy streams of their own with two sets of device buffers, so step i+1's
+    # upload and step i-1's read-back overlap step i's kernels and each other;
+    # each step still moves all of its own bytes.
+    e2e_steps = max(8, min(2 * args.steps, 12))   # enough steps that the pipeline's fill and drain stay small
     hin = [x.cpu().pin_memory() for x in (q, k, v, do)]
     hout = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
     bufs = []
@@ -351,27 +352,31 @@ def run_ours(args):
         din = [torch.empty_like(x) for x in (q, k, v, do)]
         dout_ = [torch.empty_like(x) for x in (o, lse, dq, dk, dv)]
         bufs.append((din, dout_))
-    copy_stream = torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()
-    h2d_done = [ev() for _ in range(e2e_steps)]
-    comp_done = [ev() for _ in range(e2e_steps)]
-    d2h_done = [ev() for _ in range(e2e_steps)]
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    tev = lambda: torch.cuda.Event(enable_timing=True)
+    h2d_start = [tev() for _ in range(e2e_steps)]
+    h2d_done = [tev() for _ in range(e2e_steps)]
+    comp_done = [tev() for _ in range(e2e_steps)]
+    d2h_start = [tev() for _ in range(e2e_steps)]
+    d2h_done = [tev() for _ in range(e2e_steps)]
 
     def e2e_upload(i):
         din, _ = bufs[i % 2]
-        with torch.cuda.stream(copy_stream):
+        with torch.cuda.stream(h2d_stream):
             if i >= 2:
-                copy_stream.wait_event(comp_done[i - 2])      # step i-2 no longer reads these inputs
+                h2d_stream.wait_event(comp_done[i - 2])       # step i-2 no longer reads these inputs
+            h2d_start[i].record(h2d_stream)
             for d_, h_ in zip(din, hin):
                 d_.copy_(h_, non_blocking=True)
-            h2d_done[i].record(copy_stream)
+            h2d_done[i].record(h2d_stream)
 
     barrier()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    copy_stream.wait_event(e0)
+    h2d_stream.wait_event(e0)
+    d2h_stream.wait_event(e0)
     e2e_upload(0)
     for i in range(e2e_steps):
         din, dout_ = bufs[i % 2]
@@ -385,16 +390,19 @@ def run_ours(args):
         comp_done[i].record(stream)
         if i + 1 < e2e_steps:
             e2e_upload(i + 1)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(comp_done[i])
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(comp_done[i])
+            d2h_start[i].record(d2h_stream)
             for h_, d_ in zip(hout, dout_):
                 h_.copy_(d_, non_blocking=True)
-            d2h_done[i].record(copy_stream)
+            d2h_done[i].record(d2h_stream)
     stream.wait_event(d2h_done[e2e_steps - 1])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
+    h2d_ms = sum(h2d_start[i].elapsed_time(h2d_done[i]) for i in range(e2e_steps))
+    d2h_ms = sum(d2h_start[i].elapsed_time(d2h_done[i]) for i in range(e2e_steps))
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -429,7 +437,10 @@ def run_ours(args):
                          "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
             "gpu_launches": launches_per_step * args.steps,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "copies": "pinned host buffers; copy stream overlapped with compute"},
+                    "steps": e2e_steps,
+                    "copies": "pinned host buffers; upload and read-back streams overlapped with compute",
+                    "h2d_gbs": h2d * e2e_steps / (h2d_ms * 1e-3) / 1e9,
+                    "d2h_gbs": d2h * e2e_steps / (d2h_ms * 1e-3) / 1e9},
             "clocks": clk,
             "streamed": streamed,
         }
