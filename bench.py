@@ -294,123 +294,137 @@ def run_ours(args):
     ms_step = total_ms / args.steps
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
-    # Chunk-streamed calls, as SPPO and InfiniPipe invoke attention: the forward
-    # one chunk at a time in chunk order (attn_fwd on a single chunk against the
-    # resident keys before it), the backward one chunk at a time in reverse
-    # order (attn_bwd_chunk) with fp32 dK/dV accumulators that the calls share.
-    ws_fc = cca.workspace(shape, chunks, cca.PASS_FWD, dev, per_chunk=True)
-    ws_bc = cca.workspace(shape, chunks, cca.PASS_BWD_CHUNK, dev, per_chunk=True)
-    dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=dev)
-    dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=dev)
+    def streamed_leg():
+        # Chunk-streamed calls, as SPPO and InfiniPipe invoke attention: the forward
+        # one chunk at a time in chunk order (attn_fwd on a single chunk against the
+        # resident keys before it), the backward one chunk at a time in reverse
+        # order (attn_bwd_chunk) with fp32 dK/dV accumulators that the calls share.
+        ws_fc = cca.workspace(shape, chunks, cca.PASS_FWD, dev, per_chunk=True)
+        ws_bc = cca.workspace(shape, chunks, cca.PASS_BWD_CHUNK, dev, per_chunk=True)
+        dk_acc = torch.empty_strided(k.shape, k.stride(), dtype=torch.float32, device=dev)
+        dv_acc = torch.empty_strided(v.shape, v.stride(), dtype=torch.float32, device=dev)
 
-    def streamed_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        for c in chunks:
-            cca.attn_fwd(q, k, v, [c], shape, o, lse, ws_fc, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        dk_acc.zero_()
-        dv_acc.zero_()
-        for c in reversed(chunks):
-            cca.attn_bwd_chunk(q, k, v, o, lse, do, [c], shape, dq, dk, dv, dk_acc, dv_acc, ws_bc, stream)
-        if ev is not None:
-            ev[2].record(stream)
+        def streamed_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            for c in chunks:
+                cca.attn_fwd(q, k, v, [c], shape, o, lse, ws_fc, stream)
+            if ev is not None:
+                ev[1].record(stream)
+            dk_acc.zero_()
+            dv_acc.zero_()
+            for c in reversed(chunks):
+                cca.attn_bwd_chunk(q, k, v, o, lse, do, [c], shape, dq, dk, dv, dk_acc, dv_acc, ws_bc, stream)
+            if ev is not None:
+                ev[2].record(stream)
 
-    s_steps = max(1, min(args.steps, 3))
-    streamed_step()
-    s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(s_steps)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    for i in range(s_steps):
-        streamed_step(s_ev[i])
-    torch.cuda.synchronize(dev)
-    barrier()
-    st = cca.attn_status(ws_fc, stream) or cca.attn_status(ws_bc, stream)
-    if st:
-        raise RuntimeError(f"device status after streamed steps: {cca.strerror(st)}")
-    s_fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in s_ev)
-    s_bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in s_ev)
-    streamed = {"value": world * flops_step / ((s_fwd_ms + s_bwd_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "steps": s_steps, "calls_per_step": 2 * len(chunks),
-                "fwd_tflops": flops_fwd / (s_fwd_ms * 1e-3) / 1e12, "bwd_tflops": flops_bwd / (s_bwd_ms * 1e-3) / 1e12,
-                "ms_per_step": s_fwd_ms + s_bwd_ms,
-                "note": "attn_fwd per chunk in order, attn_bwd_chunk in reverse order; zeroing of the fp32 "
-                        "dK/dV accumulators included"}
-    del dk_acc, dv_acc, ws_fc, ws_bc
+        s_steps = max(1, min(args.steps, 3))
+        streamed_step()
+        s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(s_steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(s_steps):
+            streamed_step(s_ev[i])
+        torch.cuda.synchronize(dev)
+        barrier()
+        st = cca.attn_status(ws_fc, stream) or cca.attn_status(ws_bc, stream)
+        if st:
+            raise RuntimeError(f"device status after streamed steps: {cca.strerror(st)}")
+        s_fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in s_ev)
+        s_bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in s_ev)
+        streamed = {"value": world * flops_step / ((s_fwd_ms + s_bwd_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "steps": s_steps, "calls_per_step": 2 * len(chunks),
+                    "fwd_tflops": flops_fwd / (s_fwd_ms * 1e-3) / 1e12, "bwd_tflops": flops_bwd / (s_bwd_ms * 1e-3) / 1e12,
+                    "ms_per_step": s_fwd_ms + s_bwd_ms,
+                    "note": "attn_fwd per chunk in order, attn_bwd_chunk in reverse order; zeroing of the fp32 "
+                            "dK/dV accumulators included"}
+        del dk_acc, dv_acc, ws_fc, ws_bc
+        return streamed
 
-    # End to end through the public API: every step uploads its inputs from pinned
-    # host memory and reads its results back. Uploads and read-backs run on two
-    # copy streams of their own with two sets of device buffers, so step i+1's
-    # upload and step i-1's read-back overlap step i's kernels and each other;
-    # each step still moves all of its own bytes.
-    e2e_steps = max(8, min(2 * args.steps, 12))   # enough steps that the pipeline's fill and drain stay small
-    hin = [x.cpu().pin_memory() for x in (q, k, v, do)]
-    hout = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
-    bufs = []
-    for _ in range(2):
-        din = [torch.empty_like(x) for x in (q, k, v, do)]
-        dout_ = [torch.empty_like(x) for x in (o, lse, dq, dk, dv)]
-        bufs.append((din, dout_))
-    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    tev = lambda: torch.cuda.Event(enable_timing=True)
-    h2d_start = [tev() for _ in range(e2e_steps)]
-    h2d_done = [tev() for _ in range(e2e_steps)]
-    comp_done = [tev() for _ in range(e2e_steps)]
-    d2h_start = [tev() for _ in range(e2e_steps)]
-    d2h_done = [tev() for _ in range(e2e_steps)]
+    def e2e_leg():
+        # End to end through the public API: every step uploads its inputs from pinned
+        # host memory and reads its results back. Uploads and read-backs run on two
+        # copy streams of their own with two sets of device buffers, so step i+1's
+        # upload and step i-1's read-back overlap step i's kernels and each other;
+        # each step still moves all of its own bytes.
+        e2e_steps = max(8, min(2 * args.steps, 12))   # enough steps that the pipeline's fill and drain stay small
+        hin = [x.cpu().pin_memory() for x in (q, k, v, do)]
+        hout = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
+        bufs = []
+        for _ in range(2):
+            din = [torch.empty_like(x) for x in (q, k, v, do)]
+            dout_ = [torch.empty_like(x) for x in (o, lse, dq, dk, dv)]
+            bufs.append((din, dout_))
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        tev = lambda: torch.cuda.Event(enable_timing=True)
+        h2d_start = [tev() for _ in range(e2e_steps)]
+        h2d_done = [tev() for _ in range(e2e_steps)]
+        comp_done = [tev() for _ in range(e2e_steps)]
+        d2h_start = [tev() for _ in range(e2e_steps)]
+        d2h_done = [tev() for _ in range(e2e_steps)]
 
-    def e2e_upload(i):
-        din, _ = bufs[i % 2]
-        with torch.cuda.stream(h2d_stream):
+        def e2e_upload(i):
+            din, _ = bufs[i % 2]
+            with torch.cuda.stream(h2d_stream):
+                if i >= 2:
+                    h2d_stream.wait_event(comp_done[i - 2])       # step i-2 no longer reads these inputs
+                h2d_start[i].record(h2d_stream)
+                for d_, h_ in zip(din, hin):
+                    d_.copy_(h_, non_blocking=True)
+                h2d_done[i].record(h2d_stream)
+
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d_stream.wait_event(e0)
+        d2h_stream.wait_event(e0)
+        e2e_upload(0)
+        for i in range(e2e_steps):
+            din, dout_ = bufs[i % 2]
+            q2, k2, v2, do2 = din
+            o2, lse2, dq2, dk2, dv2 = dout_
+            stream.wait_event(h2d_done[i])
             if i >= 2:
-                h2d_stream.wait_event(comp_done[i - 2])       # step i-2 no longer reads these inputs
-            h2d_start[i].record(h2d_stream)
-            for d_, h_ in zip(din, hin):
-                d_.copy_(h_, non_blocking=True)
-            h2d_done[i].record(h2d_stream)
+                stream.wait_event(d2h_done[i - 2])               # step i-2's results are read back
+            cca.attn_fwd(q2, k2, v2, chunks, shape, o2, lse2, ws_f, stream)
+            cca.attn_bwd(q2, k2, v2, o2, lse2, do2, chunks, shape, dq2, dk2, dv2, ws_b, stream)
+            comp_done[i].record(stream)
+            if i + 1 < e2e_steps:
+                e2e_upload(i + 1)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(comp_done[i])
+                d2h_start[i].record(d2h_stream)
+                for h_, d_ in zip(hout, dout_):
+                    h_.copy_(d_, non_blocking=True)
+                d2h_done[i].record(d2h_stream)
+        stream.wait_event(d2h_done[e2e_steps - 1])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        h2d_ms = sum(h2d_start[i].elapsed_time(h2d_done[i]) for i in range(e2e_steps))
+        d2h_ms = sum(d2h_start[i].elapsed_time(d2h_done[i]) for i in range(e2e_steps))
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        nbytes = lambda x: x.numel() * x.element_size()
+        h2d = sum(nbytes(x) for x in (q, k, v, do))
+        d2h = sum(nbytes(x) for x in (o, lse, dq, dk, dv))
+        e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+        return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "copies": "pinned host buffers; upload and read-back streams overlapped with compute",
+                "h2d_gbs": h2d * e2e_steps / (h2d_ms * 1e-3) / 1e9,
+                "d2h_gbs": d2h * e2e_steps / (d2h_ms * 1e-3) / 1e9}
 
-    barrier()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    h2d_stream.wait_event(e0)
-    d2h_stream.wait_event(e0)
-    e2e_upload(0)
-    for i in range(e2e_steps):
-        din, dout_ = bufs[i % 2]
-        q2, k2, v2, do2 = din
-        o2, lse2, dq2, dk2, dv2 = dout_
-        stream.wait_event(h2d_done[i])
-        if i >= 2:
-            stream.wait_event(d2h_done[i - 2])               # step i-2's results are read back
-        cca.attn_fwd(q2, k2, v2, chunks, shape, o2, lse2, ws_f, stream)
-        cca.attn_bwd(q2, k2, v2, o2, lse2, do2, chunks, shape, dq2, dk2, dv2, ws_b, stream)
-        comp_done[i].record(stream)
-        if i + 1 < e2e_steps:
-            e2e_upload(i + 1)
-        with torch.cuda.stream(d2h_stream):
-            d2h_stream.wait_event(comp_done[i])
-            d2h_start[i].record(d2h_stream)
-            for h_, d_ in zip(hout, dout_):
-                h_.copy_(d_, non_blocking=True)
-            d2h_done[i].record(d2h_stream)
-    stream.wait_event(d2h_done[e2e_steps - 1])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    h2d_ms = sum(h2d_start[i].elapsed_time(h2d_done[i]) for i in range(e2e_steps))
-    d2h_ms = sum(d2h_start[i].elapsed_time(d2h_done[i]) for i in range(e2e_steps))
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    nbytes = lambda x: x.numel() * x.element_size()
-    h2d = sum(nbytes(x) for x in (q, k, v, do))
-    d2h = sum(nbytes(x) for x in (o, lse, dq, dk, dv))
-    e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    # --device-only (large workloads whose second set of e2e buffers would not fit,
+    # or whose chunk-streamed leg would take minutes) reports the device leg alone
+    skipped = {"skipped": "--device-only"}
+    streamed = skipped if args.device_only else streamed_leg()
+    e2e = skipped if args.device_only else e2e_leg()
 
     peaks, peak_src = load_peaks()
     dom = "bwd_tiles"
@@ -436,11 +450,7 @@ def run_ours(args):
                          "frac_of_burst": achieved / peak_burst, "traffic": measured_traffic(w.name),
                          "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
             "gpu_launches": launches_per_step * args.steps,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps,
-                    "copies": "pinned host buffers; upload and read-back streams overlapped with compute",
-                    "h2d_gbs": h2d * e2e_steps / (h2d_ms * 1e-3) / 1e9,
-                    "d2h_gbs": d2h * e2e_steps / (d2h_ms * 1e-3) / 1e9},
+            "e2e": e2e,
             "clocks": clk,
             "streamed": streamed,
         }
@@ -463,6 +473,8 @@ def main():
     ap.add_argument("--workload", default="7b_128k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--device-only", action="store_true",
+                    help="report the device-timed leg only (no chunk-streamed and no end-to-end leg)")
     ap.add_argument("--plan", default="default",
                     help="default (the workload's plan) or multiplex:PP (SPPO Table 3 edge re-splits)")
     args = ap.parse_args()
