@@ -163,6 +163,11 @@ bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
 // Rank-3 TMA map of the fp32 dQ accumulator [B*H][rows][D]: box of 32 floats
 // (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
 bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);
+// Rank-4 TMA map of an fp32 dK or dV accumulator with the key/value strides of
+// gkv (element offsets of dk/dv): box of 32 floats (128 bytes, 128-byte
+// swizzle) x 128 tokens, used for reduce-adds. Fills `mp` (same axis order as
+// the bf16 key/value maps).
+bool make_kv_acc_map(CUtensorMap* m, float* acc, const Geom& gkv, TcMaps& mp);
 int device_sm_count();
 
 // Key-range boundaries cb = k_0 < ... < k_P = qe of a chunk re-split into P

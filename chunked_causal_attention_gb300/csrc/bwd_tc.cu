@@ -31,7 +31,9 @@
 //                TMEM columns as bf16 (A operands of dV, dK); dS also goes to
 //                shared memory for dQ. The MMA thread consumes chunks as they
 //                are released. At the end of the item warps 4-7 write dK*scale
-//                and warps 8-11 write dV.
+//                and warps 8-11 write dV; in the chunk-streamed backward a tile
+//                whose keys are all context adds them into the fp32 accumulators
+//                by TMA reduce-adds staged through the dS buffer.
 //   warps 12-15  dQ drain, one query row per thread: dQ*scale from TMEM into the
 //                block's Q/dO stage (free once the block's MMAs are done; the
 //                fp32 tile is exactly its size), then one thread issues TMA
@@ -157,18 +159,28 @@ __device__ __forceinline__ void sg_block(uint32_t tm, int grp, int krow, int key
     }
 }
 
+// TMA maps of the fp32 dK/dV accumulators, a kernel parameter only in the
+// chunk-streamed instantiations.
+template <bool ACC>
+struct AccMaps {};
+template <>
+struct AccMaps<true> {
+    CUtensorMap dk, dv;
+};
+
 // GROUPED: key/value heads shared by several query heads. The ungrouped
 // instantiation has G = 1 at compile time, which keeps the per-block walk of
 // the softmax-gradient warps as light as it was before grouping existed.
 // PAD: the head dim is below the tile width D (its dims past it load as zeros
 // and are not written); the unpadded instantiations keep every write bound at
-// compile time.
-template <int D, bool GROUPED, bool PAD>
+// compile time. ACC: the chunk-streamed backward (fp32 dK/dV accumulators); the
+// whole backward is compiled without its epilogue paths.
+template <int D, bool GROUPED, bool PAD, bool ACC>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                  const __grid_constant__ CUtensorMap tmdq, const BwdArgs a, const TcMaps mp, const TcMaps mpkv,
-                  const int32_t n_work) {
+                  const __grid_constant__ CUtensorMap tmdq, const __grid_constant__ AccMaps<ACC> am,
+                  const BwdArgs a, const TcMaps mp, const TcMaps mpkv, const int32_t n_work) {
     using LY = BwdTcLayout<D>;
     constexpr uint32_t kColDK = kColDV + D;
     extern __shared__ uint8_t smem_raw[];
@@ -406,9 +418,50 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(grp == 0 ? a.dk : a.dv) + roff;
             // chunk-streamed backward: add into the fp32 accumulator row, and write
             // bf16 only for the chunk's own keys (complete once their chunk has run)
-            float* acc = a.dk_acc ? (grp == 0 ? a.dk_acc : a.dv_acc) + roff : nullptr;
+            float* acc = ACC ? (grp == 0 ? a.dk_acc : a.dv_acc) + roff : nullptr;
             const bool emit = acc == nullptr || key >= item.emit_from;
             const int Dv = PAD ? a.g.D : D;        // dims written (the tile's dims past the head dim are zero)
+            if (ACC && item.emit_from >= item.j1) {
+                // Every key of this tile is context of the call's rows, so only the fp32
+                // accumulators change: stage 32 columns at a time in this group's half of
+                // the dS buffer (free until this group's next softmax gradient) and add
+                // them with a TMA reduce-add; the TMA unit does the read-modify-write in
+                // L2. Rows past the tile's last key hold zeros (their P and dS are zero).
+                uint8_t* stg_row = sm + LY::DS_OFF + grp * 16384 + krow * 128;
+                const uint32_t stg = sbase + LY::DS_OFF + grp * 16384;
+                const CUtensorMap* amap = nullptr;
+                if constexpr (ACC) amap = grp == 0 ? &am.dk : &am.dv;
+                const int c1 = mpkv.pos_t == 1 ? item.j0 : (mpkv.pos_h == 1 ? hk : b);
+                const int c2 = mpkv.pos_t == 2 ? item.j0 : (mpkv.pos_h == 2 ? hk : b);
+                const int c3 = mpkv.pos_t == 3 ? item.j0 : (mpkv.pos_h == 3 ? hk : b);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    if (PAD && c * 32 >= Dv) break;    // the same for every thread of the group
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + col + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 v = live ? make_float4(__uint_as_float(r[4 * u]) * gmul,
+                                                            __uint_as_float(r[4 * u + 1]) * gmul,
+                                                            __uint_as_float(r[4 * u + 2]) * gmul,
+                                                            __uint_as_float(r[4 * u + 3]) * gmul)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4*>(stg_row + ((u ^ (krow & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();
+                    named_sync(1 + grp, 128);
+                    if (krow == 0) {
+                        tma_reduce_add_4d(amap, stg, c * 32, c1, c2, c3);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
+                    named_sync(1 + grp, 128);          // the staging may be rewritten
+                }
+                tc_fence_before();
+                mbar_arrive(bar(LY::B_DKDVFREE));
+                continue;
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -447,6 +500,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(LY::B_DKDVFREE));
         }
+        if (ACC && krow == 0) bulk_wait_all();          // accumulator reduce-adds complete
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain
         const int qrow = tid - 384;
@@ -533,7 +587,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     }
 }
 
-template <int D, bool GROUPED, bool PAD>
+template <int D, bool GROUPED, bool PAD, bool ACC>
 cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
@@ -542,27 +596,43 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
         !make_tile_map(&mv, a.v, gkv, mpkv) || !make_tile_map(&mdo, a.dout, a.g, mp) ||
         !make_dq_acc_map(&mdq, a.dq_acc, a.g, a.rows))
         return cudaErrorInvalidValue;
+    // fp32 dK/dV accumulators of the chunk-streamed backward (unused otherwise);
+    // they have the key/value strides, so their axis order is that of mpkv
+    AccMaps<ACC> am;
+    if constexpr (ACC) {
+        TcMaps mpa{1, 2, 3};
+        if (!make_kv_acc_map(&am.dk, a.dk_acc, gkv, mpa) || !make_kv_acc_map(&am.dv, a.dv_acc, gkv, mpa) ||
+            mpa.pos_t != mpkv.pos_t || mpa.pos_h != mpkv.pos_h)
+            return cudaErrorInvalidValue;
+    }
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.Hkv;
     if (work <= 0) return cudaSuccess;
     if (work > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = BwdTcLayout<D>::ALLOC;
     cudaError_t e =
-        cudaFuncSetAttribute(bwd_tc_kernel<D, GROUPED, PAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(bwd_tc_kernel<D, GROUPED, PAD, ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_tc_kernel<D, GROUPED, PAD><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
+    bwd_tc_kernel<D, GROUPED, PAD, ACC><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, am, a, mp, mpkv,
+                                                                        (int32_t)work);
     return cudaGetLastError();
+}
+
+// Head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles.
+template <bool ACC>
+cudaError_t launch_variant(const BwdArgs& a, cudaStream_t s) {
+    const bool grouped = a.g.Hkv != a.g.H;
+    if (a.g.D == 128) return grouped ? launch_d<128, true, false, ACC>(a, s) : launch_d<128, false, false, ACC>(a, s);
+    if (a.g.D == 64) return grouped ? launch_d<64, true, false, ACC>(a, s) : launch_d<64, false, false, ACC>(a, s);
+    if (a.g.D > 64) return grouped ? launch_d<128, true, true, ACC>(a, s) : launch_d<128, false, true, ACC>(a, s);
+    return grouped ? launch_d<64, true, true, ACC>(a, s) : launch_d<64, false, true, ACC>(a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s) {
-    // head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles
-    const bool grouped = a.g.Hkv != a.g.H;
-    if (a.g.D == 128) return grouped ? launch_d<128, true, false>(a, s) : launch_d<128, false, false>(a, s);
-    if (a.g.D == 64) return grouped ? launch_d<64, true, false>(a, s) : launch_d<64, false, false>(a, s);
-    if (a.g.D > 64) return grouped ? launch_d<128, true, true>(a, s) : launch_d<128, false, true>(a, s);
-    return grouped ? launch_d<64, true, true>(a, s) : launch_d<64, false, true>(a, s);
+    return a.dk_acc != nullptr ? launch_variant<true>(a, s) : launch_variant<false>(a, s);
 }
 
 }  // namespace attn

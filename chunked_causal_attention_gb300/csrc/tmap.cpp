@@ -22,7 +22,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) {
+// Rank-4 map of a [B, T, H, D]-strided tensor (axes 1..3 sorted by stride),
+// box = box_cols elements of the head dim x 128 tokens, 128-byte swizzle.
+static bool make_map4(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, CUtensorMapDataType dt,
+                      int elem_bytes, int box_cols) {
     auto enc = encode_fn();
     if (!enc) return false;
     struct Ax {
@@ -38,11 +41,11 @@ bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) 
             }
     cuuint64_t dims[4] = {(cuuint64_t)g.D, 0, 0, 0};
     cuuint64_t strides[3];
-    cuuint32_t box[4] = {64, 1, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)box_cols, 1, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     for (int i = 0; i < 3; ++i) {
         dims[i + 1] = (cuuint64_t)ax[i].dim;
-        strides[i] = (cuuint64_t)ax[i].stride * 2;
+        strides[i] = (cuuint64_t)ax[i].stride * (cuuint64_t)elem_bytes;
         if (ax[i].which == 0) {
             box[i + 1] = 128;
             mp.pos_t = i + 1;
@@ -52,10 +55,17 @@ bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) 
             mp.pos_b = i + 1;
         }
     }
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) {
+    return make_map4(m, base, g, mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64);
+}
+
+bool make_kv_acc_map(CUtensorMap* m, float* acc, const Geom& gkv, TcMaps& mp) {
+    return make_map4(m, acc, gkv, mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32);
 }
 
 bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows) {
