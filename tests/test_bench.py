@@ -1,0 +1,65 @@
+"""Host-side checks of bench.py (no GPU): the oracle arm's JSON line, the
+gating of the committed ncu traffic record by the kernel sources' hash, and
+the workload config keys."""
+import json
+import os
+import subprocess
+import sys
+import types
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--workload", "7b_32k"], capture_output=True, text=True, cwd=ROOT,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["dtype"] == "f64"
+    assert d["config"]["workload"] == "7b_32k"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_traffic_record_is_gated_by_source_hash(tmp_path, monkeypatch):
+    rec = {"workload": "7b_128k", "dram_bytes_read": 3.0, "dram_bytes_write": 4.0,
+           "source_sha256": bench.kernel_source_hash()}
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(p))
+    assert bench.measured_traffic("7b_128k") == 7.0
+    assert bench.measured_traffic("7b_32k") is None              # another workload
+    rec["source_sha256"] = "0" * 64                               # kernel changed since the capture
+    p.write_text(json.dumps(rec))
+    assert bench.measured_traffic("7b_128k") is None
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(tmp_path / "missing.json"))
+    assert bench.measured_traffic("7b_128k") is None
+
+
+def test_committed_traffic_record_names_its_kernel_and_command():
+    with open(os.path.join(ROOT, "profiles", "traffic_7b_128k.json")) as f:
+        rec = json.load(f)
+    assert rec["workload"] == "7b_128k" and len(rec["source_sha256"]) == 64
+    assert rec["dram_bytes_read"] > 0 and rec["dram_bytes_write"] > 0
+    assert "--clock-control none" in rec["command"] and "bwd_tc_kernel" in rec["kernel"]
+
+
+@pytest.mark.parametrize("name", ["tiny", "7b_32k", "7b_128k", "packed_256k", "13b_1m", "gqa_128k"])
+def test_workload_config(name):
+    from chunked_causal_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    args = types.SimpleNamespace(gpus=1, plan="default")
+    cfg = bench.workload_config(w, args)
+    assert cfg["workload"] == name and cfg["D"] == w.D and cfg["H"] == w.H and cfg["packed"] == w.packed
+    assert "model" not in cfg
+    if w.Hkv is not None:
+        assert cfg["Hkv"] == w.Hkv
