@@ -167,15 +167,16 @@ def run_reference(args):
         return
     from chunked_causal_attention_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    n_tok = args.cpu_sample_tokens
     for i in range(args.warmup):
-        time_oracle_sample(w, CPU_SAMPLE_TOKENS // 4, 7000 + i)
+        time_oracle_sample(w, max(128, n_tok // 4), 7000 + i)
     vals, secs = [], []
     for i in range(args.steps):
-        v, dt = time_oracle_sample(w, CPU_SAMPLE_TOKENS, 8000 + i)
+        v, dt = time_oracle_sample(w, n_tok, 8000 + i)
         vals.append(v)
         secs.append(dt)
     value = statistics.median(vals)
-    sample = (f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of {CPU_SAMPLE_TOKENS} tokens "
+    sample = (f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of {n_tok} tokens "
               f"of one head (D={w.D}) per step; TFLOP/s = 14*D*pairs/time")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
@@ -334,7 +335,8 @@ def run_ours(args):
         s_bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in s_ev)
         streamed = {"value": world * flops_step / ((s_fwd_ms + s_bwd_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "steps": s_steps, "calls_per_step": 2 * len(chunks),
-                    "fwd_tflops": flops_fwd / (s_fwd_ms * 1e-3) / 1e12, "bwd_tflops": flops_bwd / (s_bwd_ms * 1e-3) / 1e12,
+                    "fwd_tflops": flops_fwd / (s_fwd_ms * 1e-3) / 1e12,
+                    "bwd_tflops": flops_bwd / (s_bwd_ms * 1e-3) / 1e12,
                     "ms_per_step": s_fwd_ms + s_bwd_ms,
                     "note": "attn_fwd per chunk in order, attn_bwd_chunk in reverse order; zeroing of the fp32 "
                             "dK/dV accumulators included"}
@@ -455,11 +457,11 @@ def run_ours(args):
             "streamed": streamed,
         }
         if world == 1 and not args.no_cpu_baseline:
-            v_cpu, dt = time_oracle_sample(w, CPU_SAMPLE_TOKENS, 9000)
+            v_cpu, dt = time_oracle_sample(w, args.cpu_sample_tokens, 9000)
             line["cpu_baseline"] = {
                 "value": v_cpu, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                "sample": f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of {CPU_SAMPLE_TOKENS} "
-                          f"tokens of one head, {dt:.1f} s"}
+                "sample": f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of "
+                          f"{args.cpu_sample_tokens} tokens of one head, {dt:.1f} s"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -473,6 +475,8 @@ def main():
     ap.add_argument("--workload", default="7b_128k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=CPU_SAMPLE_TOKENS,
+                    help="causal prefix that the oracle (cpu_baseline, reference arm) is timed on")
     ap.add_argument("--device-only", action="store_true",
                     help="report the device-timed leg only (no chunk-streamed and no end-to-end leg)")
     ap.add_argument("--plan", default="default",

@@ -16,8 +16,8 @@ import bench  # noqa: E402
 
 def test_reference_arm_prints_one_json_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                        "--warmup", "0", "--workload", "7b_32k"], capture_output=True, text=True, cwd=ROOT,
-                       timeout=600)
+                        "--warmup", "0", "--workload", "7b_32k", "--cpu-sample-tokens", "2048"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -63,3 +63,22 @@ def test_workload_config(name):
     assert "model" not in cfg
     if w.Hkv is not None:
         assert cfg["Hkv"] == w.Hkv
+
+
+def test_reference_arm_under_torchrun_prints_from_rank_0_only():
+    """The driver launches N > 1 through torchrun: rank 0 alone runs the oracle
+    arm and prints its line, the other ranks exit 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "7b_32k",
+                        "--cpu-sample-tokens", "2048"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
