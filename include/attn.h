@@ -45,7 +45,11 @@
  *   - lse: fp32, [B][H][T] contiguous, natural log.
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Compute calls only enqueue work and return before it completes.
- *   - chunks: a HOST array read during the call only.
+ *   - chunks: a HOST array read during the call only. Each compute call lays
+ *     out its work list on the host and copies it into the workspace with
+ *     cudaMemcpyAsync on `stream` from host memory that is released when the
+ *     call returns, so the calls are not meant for CUDA graph stream capture:
+ *     a replayed copy would read released memory.
  *   - Every call returns an attn status code. Argument errors are detected on
  *     the host before anything is enqueued. Device-side errors (a bounded wait
  *     that gave up, an index check that failed) are recorded in the workspace

@@ -11,7 +11,7 @@ from chunked_causal_attention_gb300.workloads import WORKLOADS, make_inputs, wor
 from oracle import attention as A
 from oracle import plan as P
 
-from parity import check_fwd, check_grad, default_scale, docs_of, head, lse_head, run_gpu
+from parity import check_fwd, check_grad, default_scale, docs_of, head, lse_head, rel_l2, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -256,3 +256,34 @@ def test_head_dim_padding_leaves_neighbours_untouched():
         assert torch.all(g[..., D:] == 3.0)
     o, lse2, dq, dk, dv = full_check(*views, chunks, False, what="D80 in a 128-wide buffer")
     assert torch.equal(o_buf[..., :D], o) and torch.equal(lse, lse2)
+
+
+def test_concurrent_calls_on_two_streams():
+    """The library keeps no mutable state between calls: two problems run at
+    the same time on two streams, each with its own workspace, give what
+    they give one after the other (O, LSE, dK, dV bit for bit; dQ, whose fp32
+    reduce-adds run in any order, within the tolerance)."""
+    cases = [(1, 4, 3000, 128, P.plan(3000, 3, P.FLOPS_RESPLIT_EDGES), 401),
+             (2, 3, 2000, 64, P.plan(2000, 2, P.FLOPS), 402)]
+    inputs = [[x.cuda() for x in make_inputs(B, H, L, D, seed=sd)] for B, H, L, D, _, sd in cases]
+    serial = []
+    for (q, k, v, do), c in zip(inputs, cases):
+        o, lse = cca.forward(q, k, v, c[4])
+        dq, dk, dv = cca.backward(q, k, v, o, lse, do, c[4])
+        serial.append((o, lse, dq, dk, dv))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [None, None]
+    for rep in range(3):
+        for i, ((q, k, v, do), c) in enumerate(zip(inputs, cases)):
+            with torch.cuda.stream(streams[i]):
+                o, lse = cca.forward(q, k, v, c[4], stream=streams[i])
+                dq, dk, dv = cca.backward(q, k, v, o, lse, do, c[4], stream=streams[i])
+                outs[i] = (o, lse, dq, dk, dv)
+        torch.cuda.synchronize()
+        for i in range(2):
+            o, lse, dq, dk, dv = outs[i]
+            so, slse, sdq, sdk, sdv = serial[i]
+            assert torch.equal(o, so) and torch.equal(lse, slse), (rep, i)
+            assert torch.equal(dk, sdk) and torch.equal(dv, sdv), (rep, i)
+            assert rel_l2(dq.float().cpu().numpy(), sdq.float().cpu().numpy()) < 1e-3, (rep, i)
