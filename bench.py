@@ -154,6 +154,11 @@ def time_oracle_sample(w, tokens, seed):
     return 14 * D * pairs / dt / 1e12, dt
 
 
+def workload_flops(w):
+    """Algorithmic fwd+bwd FLOPs of a workload: 14 D per visible pair (per document when packed)."""
+    return 14 * w.D * causal_pairs_total(w, None)
+
+
 def cpu_cores():
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(var, "").isdigit():
@@ -183,7 +188,9 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w, args),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample,
+                             "extrapolated_full_step_s": workload_flops(w) / (value * 1e12),
+                             "extrapolation": "the workload's fwd+bwd FLOPs at the sample's rate (not measured)"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -461,7 +468,9 @@ def run_ours(args):
             line["cpu_baseline"] = {
                 "value": v_cpu, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                 "sample": f"oracle.attention.backward (float64 fwd+bwd) on a causal prefix of "
-                          f"{args.cpu_sample_tokens} tokens of one head, {dt:.1f} s"}
+                          f"{args.cpu_sample_tokens} tokens of one head, {dt:.1f} s",
+                "extrapolated_full_step_s": flops_step / (v_cpu * 1e12),
+                "extrapolation": "the workload's fwd+bwd FLOPs at the sample's rate (not measured)"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -27,6 +27,10 @@ def test_reference_arm_prints_one_json_line():
     assert d["config"]["workload"] == "7b_32k"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1
+    from chunked_causal_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS["7b_32k"]
+    full = 14 * w.D * w.H * w.L * (w.L + 1) // 2
+    assert abs(d["cpu_baseline"]["extrapolated_full_step_s"] - full / (d["value"] * 1e12)) < 1e-6 * full / (d["value"] * 1e12)
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
