@@ -12,6 +12,8 @@
 // dQ accumulator rows are reused from L2. With grouped key/value heads (GQA/MQA)
 // an item is a key tile of one key/value head and walks the query blocks of
 // each of its H / Hkv query heads in turn, so dK/dV collect the group's sum.
+// The tiles are D = 64 or 128 dims wide; a head dim below D loads its
+// remaining dims as zeros and only its own dims are written (PAD).
 //
 // Warp roles (16 warps):
 //   warp 0       TMA producer: K, V once per item; Q and dO of a query block into

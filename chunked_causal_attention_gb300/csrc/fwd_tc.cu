@@ -1,7 +1,9 @@
 // Forward tile kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Persistent CTAs walk the cost-sorted work list (128 query rows x one key
-// range x one (batch, head)). Warp roles:
+// range x one (batch, head)). The tiles are D = 64 or 128 dims wide; a head
+// dim below D loads its remaining dims as zeros (the TMA maps carry the true
+// head dim) and only its own dims are written. Warp roles:
 //   warp 0      TMA producer: Q tile once per item; K and V tiles of 128 keys
 //               through two-stage rings (128-byte swizzled, 64-column boxes),
 //               from the key/value head of the item's query head (grouped
