@@ -337,3 +337,47 @@ def test_compute_wrappers_reject_cpu_and_mismatched_tensors():
     with pytest.raises(cca.AttnError) as e:
         cca.attn_bwd_chunk(q, q, q, q, lse, q, ch, s, q, q, q, q.float(), q.float(), ws)
     assert e.value.status == 1
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/attn.h is a C header: a C99 program that includes it, links
+    libattn.so and calls the host-only entry points (planner, workspace size,
+    error strings, version) compiles and gives the same plan as the binding."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(ROOT, "include")
+    src = tmp_path / "use_attn.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "attn.h"
+int main(void) {
+    attn_chunk c[16];
+    int32_t n = 0;
+    if (attn_plan(131072, 16, ATTN_PLAN_FLOPS_RESPLIT_EDGES, c, 16, &n) != ATTN_OK) return 1;
+    attn_shape s = {1, 32, 131072, 128, 32LL * 131072 * 128, 128, 131072LL * 128, 0.08838834764831845f, 0, 0, 0, 0};
+    size_t bytes = 0;
+    if (attn_workspace_size(&s, c, n, 1, &bytes) != ATTN_OK || bytes == 0) return 2;
+    s.D = 100;
+    if (attn_workspace_size(&s, c, n, 1, &bytes) != ATTN_E_UNSUPPORTED) return 3;
+    printf("%d", (int)n);
+    for (int32_t i = 0; i < n; ++i) printf(" %d,%d,%d,%d", c[i].q_begin, c[i].q_end, c[i].ctx_begin, c[i].kv_split);
+    printf("\n%s\n%s\n", attn_strerror(ATTN_E_UNSUPPORTED), attn_version());
+    return 0;
+}
+''')
+    exe = tmp_path / "use_attn"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-L", libdir, "-lattn",
+                        f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    lines = out.stdout.splitlines()
+    fields = lines[0].split()
+    got = [tuple(int(x) for x in f.split(",")) for f in fields[1:]]
+    assert int(fields[0]) == len(got) == 16
+    assert got == cca.attn_plan(131072, 16, cca.PLAN_FLOPS_RESPLIT_EDGES)
+    assert lines[1] == cca.strerror(3) and lines[2]
