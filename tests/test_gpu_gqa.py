@@ -134,3 +134,18 @@ def test_gqa_128k_sampled():
         sv = head(dv, 0, hk, False).sum(axis=0) - sdo
         norm = np.sqrt(sum((head(do, 0, h, False) ** 2).sum() for h in range(hk * G, hk * G + G)))
         assert np.linalg.norm(sv) / norm <= 5e-3
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_grouped_p_part_plan(D):
+    """Grouped key/value heads with a plan whose edge chunks are re-split into
+    P key parts: the forward partials and their merge per query head, the
+    backward's group sums."""
+    L = 3000
+    chunks = cca.attn_plan_multiplex(L, 6, 4)
+    assert any(c[3] < 0 for c in chunks)
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 8, L, D, seed=520 + D, Hkv=2))
+    o, lse = cca.forward(q, k, v, chunks)
+    dq, dk, dv = cca.backward(q, k, v, o, lse, do, chunks)
+    torch.cuda.synchronize()
+    grouped_check(q, k, v, do, o, lse, dq, dk, dv, None, False, f"gqa multiplex D{D}")

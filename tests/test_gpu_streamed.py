@@ -197,3 +197,13 @@ def test_streamed_head_dims_between_tile_widths(D):
     chunks = P.plan(1000, 4, P.FLOPS_RESPLIT_EDGES)
     q, k, v, do = (x.cuda() for x in make_inputs(2, 2, 1000, D, seed=310 + D))
     streamed_check(q, k, v, do, chunks, False, f"streamed D{D}")
+
+
+@pytest.mark.parametrize("L,N,PP", [(3000, 6, 4), (2600, 4, 3)])
+def test_streamed_p_part_plan(L, N, PP):
+    """Chunk-streamed calls of a plan whose edge chunks are re-split into P
+    key parts (SPPO Table 3): every forward call merges its own parts."""
+    chunks = cca.attn_plan_multiplex(L, N, PP)
+    assert chunks == P.plan_multiplex(L, N, PP) and any(c[3] < 0 for c in chunks)
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 2, L, 128, seed=320 + L + PP))
+    streamed_check(q, k, v, do, chunks, False, f"streamed multiplex L{L} N{N} PP{PP}")
