@@ -5,6 +5,7 @@
   equal-cost point solved with 50-digit decimal square roots.
 * A packing worked out by hand from the algorithm's steps.
 * The loosening reading: a bucket that is full of tokens never blocks.
+* The bucket order: increasing tot_time/tot_tokens, ties to the older bucket.
 * Invariants on random inputs: every token in exactly one chunk, one call
   never holds two slices of a sequence, at most one tail per bucket, token
   and time thresholds respected, split slices equal to the mesh.
@@ -110,6 +111,24 @@ def test_loosening_skips_buckets_full_of_tokens():
     T_t = IP.bfd([a, b], [(2, 20)], T_t=150.0, T_m=100, cost=cost)
     assert T_t == 500.0 + 400.0
     assert b.members[-1] == (2, 0, 20) and a.members == [(0, 0, 90)]
+
+
+def test_bucket_order_is_increasing_time_per_token():
+    """Algorithm 1 visits the buckets in increasing order of tot_time/tot_tokens
+    and takes the first that fits: with two buckets that can both take the
+    sequence, the one with less time per token receives it; equal ratios go
+    to the older bucket."""
+    cost = IP.Cost(1.0, 0.0, 0.0)                          # a 10-token sequence costs 100
+    a = IP.Bucket(order=0, tail=False, members=[(0, 0, 50)], tot_time=500.0, tot_tokens=50)    # 10 per token
+    b = IP.Bucket(order=1, tail=False, members=[(1, 0, 100)], tot_time=300.0, tot_tokens=100)  # 3 per token
+    T_t = IP.bfd([a, b], [(2, 10)], T_t=1000.0, T_m=1000, cost=cost)
+    assert T_t == 1000.0
+    assert b.members[-1] == (2, 0, 10) and a.members == [(0, 0, 50)]
+    assert (b.tot_time, b.tot_tokens) == (400.0, 110)
+    c = IP.Bucket(order=0, tail=False, members=[(0, 0, 40)], tot_time=200.0, tot_tokens=40)    # 5 per token
+    d = IP.Bucket(order=1, tail=False, members=[(1, 0, 20)], tot_time=100.0, tot_tokens=20)    # 5 per token
+    IP.bfd([c, d], [(2, 10)], T_t=1000.0, T_m=1000, cost=cost)
+    assert c.members[-1] == (2, 0, 10) and d.members == [(1, 0, 20)]
 
 
 def random_case(rng):

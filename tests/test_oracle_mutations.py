@@ -174,3 +174,57 @@ def test_resplit_point_mistake_is_caught(monkeypatch):
         return m if q_begin < m < q_end else 0
     monkeypatch.setattr(P, "resplit_point", resplit_off_by_one_tile)
     assert fails(TP.test_resplit_point) or fails(TP.test_golden_plans)
+
+
+# ------------------------------------------------------------------ InfiniPipe Algorithm 1
+
+def test_infinipipe_mesh_rounding_mistake_is_caught(monkeypatch):
+    import test_oracle_infinipipe as TI
+    from oracle import infinipipe as IP
+
+    def split_longest_floor(Lmax, K, cost):
+        total = cost.prefix_cost(Lmax)
+        b = [0]
+        for k in range(1, K):
+            m = 0
+            while float(K) * cost.prefix_cost(IP.TILE * (m + 1)) <= float(k) * total:
+                m += 1
+            b.append(IP.TILE * m)                            # rounds down instead of to the nearest
+        b.append(Lmax)
+        if any(not b[i] < b[i + 1] for i in range(K)):
+            raise IP.PlanError("collapsed")
+        return b
+    monkeypatch.setattr(IP, "split_longest", split_longest_floor)
+    assert fails(TI.test_mesh_equal_cost_point, 1e-9, 3e-4) or fails(TI.test_hand_worked_packing)
+
+
+def test_infinipipe_bucket_order_mistake_is_caught(monkeypatch):
+    import test_oracle_infinipipe as TI
+    from oracle import infinipipe as IP
+
+    def bfd_most_loaded_first(buckets, shorts, T_t, T_m, cost):
+        for idx, s in shorts:
+            t = cost.slice_time(0, s)
+            while True:
+                if not buckets or min(b.tot_tokens for b in buckets) + s > T_m:
+                    nb = IP.Bucket(order=len(buckets), tail=False)
+                    nb.members.append((idx, 0, s))
+                    nb.tot_time = cost.beta1 + t
+                    nb.tot_tokens = s
+                    buckets.append(nb)
+                    break
+                placed = False
+                # buckets by decreasing tot_time/tot_tokens instead of increasing
+                for b in sorted(buckets, key=lambda x: (-x.metric(), x.order)):
+                    if b.tot_time + t <= T_t and b.tot_tokens + s <= T_m:
+                        b.members.append((idx, 0, s))
+                        b.tot_time += t
+                        b.tot_tokens += s
+                        placed = True
+                        break
+                if placed:
+                    break
+                T_t = min(b.tot_time for b in buckets if b.tot_tokens + s <= T_m) + t
+        return T_t
+    monkeypatch.setattr(IP, "bfd", bfd_most_loaded_first)
+    assert fails(TI.test_bucket_order_is_increasing_time_per_token)
