@@ -232,6 +232,10 @@ def test_plan_infinipipe_matches_oracle_exactly():
         assert got == [list(c) for c in want], (lengths, K, cap, a1, a2, b1)
         checked += 1
     assert checked > 300
+    # the hand-worked cases of the oracle's pins (bucket packing, the starting threshold)
+    for lengths, cap in (([1024, 300, 256, 200, 128, 100], 1024), ([1024, 800, 700, 100], 2048)):
+        want, _ = IP.plan(lengths, 2, cap, IP.Cost(1.0, 0.0, 0.0))
+        assert cca.attn_plan_infinipipe(lengths, 2, cap, 1.0, 0.0, 0.0) == [list(c) for c in want]
 
 
 def test_plan_infinipipe_workload_lengths():

@@ -6,6 +6,7 @@
 * A packing worked out by hand from the algorithm's steps.
 * The loosening reading: a bucket that is full of tokens never blocks.
 * The bucket order: increasing tot_time/tot_tokens, ties to the older bucket.
+* The starting threshold T_t: the costliest mesh slice, worked by hand.
 * Invariants on random inputs: every token in exactly one chunk, one call
   never holds two slices of a sequence, at most one tail per bucket, token
   and time thresholds respected, split slices equal to the mesh.
@@ -129,6 +130,32 @@ def test_bucket_order_is_increasing_time_per_token():
     d = IP.Bucket(order=1, tail=False, members=[(1, 0, 20)], tot_time=100.0, tot_tokens=20)    # 5 per token
     IP.bfd([c, d], [(2, 10)], T_t=1000.0, T_m=1000, cost=cost)
     assert c.members[-1] == (2, 0, 10) and d.members == [(1, 0, 20)]
+
+
+def test_threshold_starts_at_the_costliest_mesh_slice():
+    """T_t starts at the largest modeled time of a mesh slice. Worked by hand
+    with alpha1 = 1, alpha2 = beta1 = 0, lengths [1024, 800, 700, 100], K = 2,
+    token capacity 2048:
+      mesh [768, 256]; slice times 768^2 = 589824 and 1024^2 - 768^2 = 458752,
+      so T_t = 589824.
+      seq 0 -> (0, 768) and the tail (768, 256): bucket 0, time 458752, 256
+      tokens (1792 per token). seq 1 -> (0, 768) and the tail (768, 32):
+      bucket 1, time 800^2 - 768^2 = 50176, 32 tokens (1568 per token).
+      700 (time 490000): bucket 1 first; 540176 <= T_t -> bucket 1.
+      100 (time 10000): bucket 1 first (737.9 per token); 550176 <= T_t ->
+      bucket 1.
+    Starting at the cheapest slice (458752) would loosen T_t to 540176 for the
+    700 and send the 100 to bucket 0."""
+    cost = IP.Cost(1.0, 0.0, 0.0)
+    calls, info = IP.plan([1024, 800, 700, 100], 2, 2048, cost)
+    assert info["mesh"] == [768, 256] and info["T_t"] == 589824.0
+    assert calls == [
+        [(0, 768, 0, 0)],
+        [(1024, 1792, 1024, 0)],
+        [(768, 1024, 0, 0)],
+        [(1792, 1824, 1024, 0), (1824, 2524, 1824, 0), (2524, 2624, 2524, 0)],
+    ]
+    assert info["times"] == [589824.0, 589824.0, 458752.0, 550176.0]
 
 
 def random_case(rng):

@@ -228,3 +228,170 @@ def test_infinipipe_bucket_order_mistake_is_caught(monkeypatch):
         return T_t
     monkeypatch.setattr(IP, "bfd", bfd_most_loaded_first)
     assert fails(TI.test_bucket_order_is_increasing_time_per_token)
+
+
+# ------------------------------------------------------------------ more of the planner
+
+def test_key_pairs_mistake_is_caught(monkeypatch):
+    def key_pairs_off_by_one(q_begin, q_end, ctx_begin, K):
+        n = q_end - q_begin
+        A_ = min(K, q_begin) - ctx_begin
+        B = max(0, K - q_begin)
+        return A_ * n + B * n - B * (B + 1) // 2                 # one diagonal too few
+    monkeypatch.setattr(P, "key_pairs_before", key_pairs_off_by_one)
+    assert fails(TP.test_key_pairs_closed_form_matches_counting)
+
+
+def test_resplit_rounding_mistake_is_caught(monkeypatch):
+    def resplit_floor(q_begin, q_end, ctx_begin, Pn):
+        W = P.key_pairs_before(q_begin, q_end, ctx_begin, q_end)
+        k = [ctx_begin]
+        for p in range(1, Pn):
+            m = 0
+            while True:
+                nxt = ctx_begin + P.TILE * (m + 1)               # rounds down instead of to the nearest
+                if nxt > q_end or Pn * P.key_pairs_before(q_begin, q_end, ctx_begin, nxt) > p * W:
+                    break
+                m += 1
+            k.append(ctx_begin + P.TILE * m)
+        k.append(q_end)
+        if any(not k[i] < k[i + 1] for i in range(Pn)):
+            raise P.PlanError("collapsed")
+        return k
+    monkeypatch.setattr(P, "resplit_boundaries", resplit_floor)
+    assert (fails(TP.test_resplit_causal_chunk_closed_form, 131072, 3)
+            or fails(TP.test_resplit_context_dominated_chunk_by_hand) or fails(TP.test_plan_multiplex))
+
+
+def test_varlen_chunk_count_mistake_is_caught(monkeypatch):
+    real = P.boundaries
+
+    def boundaries_one_chunk_short(L, N, mode):                  # floor(L_d / cap) chunks, at least one
+        return real(L, max(1, N - 1) if N > 1 else N, mode)
+    monkeypatch.setattr(P, "boundaries", boundaries_one_chunk_short)
+    assert fails(TP.test_varlen_plan_structure) or fails(TP.test_golden_plans)
+
+
+# ------------------------------------------------------------------ more of the attention oracle
+
+def test_chunk_backward_mistake_is_caught(monkeypatch):
+    def chunk_backward_without_context(q, k, v, do, qb, qe, cb, scale, row_block=512):
+        # keys before the chunk dropped: context treated as absent
+        dq, dk, dv = A_chunk_backward_ref(q, k, v, do, qb, qe, qb, scale, row_block)
+        pad = np.zeros((qb - cb, dk.shape[1]))
+        return dq, np.vstack([pad, dk]), np.vstack([pad, dv])
+    A_chunk_backward_ref = A.chunk_backward
+    monkeypatch.setattr(A, "chunk_backward", chunk_backward_without_context)
+    assert fails(TA.test_chunk_backward_matches_autograd, 170, 300, 100)
+
+
+def test_grouped_backward_mistake_is_caught(monkeypatch):
+    def grouped_last_head_only(qs, k, v, dos, scale, cu_seqlens=None, row_block=512):
+        dqs, Os, Ls = [], [], []
+        for q, do in zip(qs, dos):
+            dq, dk, dv, O, L = A.backward(q, k, v, do, scale, cu_seqlens, row_block)
+            dqs.append(dq)
+            Os.append(O)
+            Ls.append(L)
+        return dqs, dk, dv, Os, Ls                               # the group's sum dropped
+    monkeypatch.setattr(A, "grouped_backward", grouped_last_head_only)
+    assert fails(TA.test_grouped_backward_matches_autograd, 4, None)
+
+
+def test_sampled_rows_mistake_is_caught(monkeypatch):
+    real = A.doc_start_of_rows
+
+    def starts_ignore_documents(T, cu_seqlens):
+        return real(T, None)                                     # every row sees from token 0
+    monkeypatch.setattr(A, "doc_start_of_rows", starts_ignore_documents)
+    assert fails(TA.test_sampled_forms_match_full)
+
+
+def test_partial_mask_mistake_is_caught(monkeypatch):
+    real = A.partial
+
+    def partial_strict(q, k, v, r0, r1, kv_lo, kv_hi, scale):
+        # a key range ending one key early: the diagonal key of the last part lost
+        return real(q, k, v, r0, r1, kv_lo, max(kv_lo, kv_hi - 1) if kv_hi == r1 else kv_hi, scale)
+    monkeypatch.setattr(A, "partial", partial_strict)
+    assert fails(TA.test_chunked_equals_unchunked, P.FLOPS)
+
+
+# ------------------------------------------------------------------ more of Algorithm 1
+
+def test_infinipipe_sharding_mistake_is_caught(monkeypatch):
+    import test_oracle_infinipipe as TI
+    from oracle import infinipipe as IP
+
+    def split_by_mesh_ge(lengths, mesh):
+        out = []
+        for L in lengths:
+            rem, ctx, slices = L, 0, []
+            for m in mesh:
+                if rem >= m:                                     # a slice equal to the remainder taken
+                    slices.append((ctx, m))
+                    ctx += m
+                    rem -= m
+                else:
+                    break
+            out.append((slices, (ctx, rem) if slices else None))
+        return out
+    monkeypatch.setattr(IP, "split_by_mesh", split_by_mesh_ge)
+    assert fails(TI.test_page_example_sharding_by_mesh)
+
+
+def test_infinipipe_cost_mistake_is_caught(monkeypatch):
+    import test_oracle_infinipipe as TI
+    from oracle import infinipipe as IP
+
+    def slice_time_without_context(self, C, s):
+        return self.alpha1 * float(s * s) + self.alpha2 * float(s)   # the context's cross term dropped
+    monkeypatch.setattr(IP.Cost, "slice_time", slice_time_without_context)
+    assert fails(TI.test_hand_worked_packing)
+
+
+def test_infinipipe_threshold_mistake_is_caught(monkeypatch):
+    import test_oracle_infinipipe as TI
+    from oracle import infinipipe as IP
+
+    def plan_threshold(lengths, K, token_cap, cost, pick):
+        # Algorithm 1 with T_t started at pick() over the mesh slices' times
+        # (the oracle takes the maximum); every other step as in the oracle
+        starts = [0]
+        for L in lengths:
+            starts.append(starts[-1] + L)
+        live = [i for i, L in enumerate(lengths) if L > 0]
+        b = IP.split_longest(max(lengths), K, cost)
+        mesh = [b[i + 1] - b[i] for i in range(K)]
+        T_t = pick(cost.beta1 + cost.slice_time(b[i], mesh[i]) for i in range(K))
+        parts = IP.split_by_mesh(lengths, mesh)
+        buckets = []
+        for i in live:
+            slices, tail = parts[i]
+            if tail is not None:
+                bk = IP.Bucket(order=len(buckets), tail=True)
+                bk.members.append((i, tail[0], tail[1]))
+                bk.tot_time = cost.beta1 + cost.slice_time(tail[0], tail[1])
+                bk.tot_tokens = tail[1]
+                buckets.append(bk)
+        shorts = sorted(((i, lengths[i]) for i in live if parts[i][1] is None),
+                        key=lambda x: (-cost.slice_time(0, x[1]), x[0]))
+        T_t = IP.bfd(buckets, shorts, T_t, token_cap, cost)
+        calls, times = [], []
+        depth = max(len(parts[i][0]) for i in live)
+        for j in range(depth):
+            for i in live:
+                if j < len(parts[i][0]):
+                    ctx, m = parts[i][0][j]
+                    calls.append([(starts[i] + ctx, starts[i] + ctx + m, starts[i], 0)])
+                    times.append(cost.beta1 + cost.slice_time(ctx, m))
+        for bk in buckets:
+            calls.append(sorted((starts[i] + ctx, starts[i] + ctx + s_, starts[i], 0) for i, ctx, s_ in bk.members))
+            times.append(bk.tot_time)
+        return calls, {"mesh": mesh, "T_t": T_t, "T_m": token_cap, "times": times}
+
+    cost = IP.Cost(1.0, 0.0, 0.0)
+    for lengths in ([1024, 300, 256, 200, 128, 100], [1024, 800, 700, 100]):   # the copy is the oracle
+        assert plan_threshold(lengths, 2, 2048, cost, max) == IP.plan(lengths, 2, 2048, cost)
+    monkeypatch.setattr(IP, "plan", lambda lengths, K, cap, cost: plan_threshold(lengths, K, cap, cost, min))
+    assert fails(TI.test_threshold_starts_at_the_costliest_mesh_slice)
