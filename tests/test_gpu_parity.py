@@ -287,3 +287,22 @@ def test_concurrent_calls_on_two_streams():
             assert torch.equal(o, so) and torch.equal(lse, slse), (rep, i)
             assert torch.equal(dk, sdk) and torch.equal(dv, sdv), (rep, i)
             assert rel_l2(dq.float().cpu().numpy(), sdq.float().cpu().numpy()) < 1e-3, (rep, i)
+
+
+def test_empty_chunk_list():
+    """No chunks: the forward enqueues nothing and leaves its outputs as they
+    were; the backward, which needs a partition of [0, T), refuses it on the
+    host (ATTN_E_INVAL) before anything is enqueued."""
+    L, H, D = 300, 2, 64
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=41))
+    shape = cca.shape_of(q)
+    ws = cca.workspace(shape, [], 0)
+    o = torch.full_like(q, 2.0)
+    lse = torch.full((1, H, L), 3.0, device="cuda")
+    cca.attn_fwd(q, k, v, [], shape, o, lse, ws)
+    torch.cuda.synchronize()
+    assert cca.attn_status(ws) == 0
+    assert torch.all(o == 2.0) and torch.all(lse == 3.0)
+    with pytest.raises(cca.AttnError) as e:
+        cca.attn_workspace_size(shape, [], 1)
+    assert e.value.status == 1
