@@ -269,8 +269,7 @@ def run_ours(args):
         raise RuntimeError(f"device status after warm-up: {cca.strerror(st)}")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(local, args.clock_log)
     clocks.start()
     time.sleep(0.3)
     barrier()
@@ -490,6 +489,8 @@ def main():
                     help="report the device-timed leg only (no chunk-streamed and no end-to-end leg)")
     ap.add_argument("--plan", default="default",
                     help="default (the workload's plan) or multiplex:PP (SPPO Table 3 edge re-splits)")
+    ap.add_argument("--clock-log", default=None,
+                    help="also write the raw nvidia-smi clock samples of the timed region to this CSV file")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -19,7 +19,7 @@ Long-Context LLM Training":
     and the token threshold T_m; open a new bucket when even the bucket with
     the fewest tokens cannot take it; loosen T_t when no bucket fits.
 
-Readings where the pages leave a step open (listed in the design doc):
+Readings where the pages leave a step open:
   * One GPU: N = 1 and d_p = 1 in Eq. (1); there is no all-to-all term (Eq. 3),
     so a chunk's modeled time is beta1 plus the sum of its slices' terms.
   * Mesh boundaries: b_k is the multiple of 128 nearest to the equal-cost

@@ -20,7 +20,7 @@ Sources
   sequence with a context C (the preceding slices); short sequences form
   batched chunks with C = 0.
 
-Readings taken where the pages leave a step open (stated in the design doc):
+Readings taken where the pages leave a step open:
 * FLOPS rule: b_k = nearest multiple of 128 to L*sqrt(k/N), ties rounded up,
   b_0 = 0, b_N = L; a plan whose boundaries are not strictly increasing is an
   error (too many chunks for L), never clamped.
