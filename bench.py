@@ -207,6 +207,22 @@ def workload_config(w, args):
 
 
 # ----------------------------------------------------------------- GPU arm
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: a job of replicas ends when its last rank does."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_replica_step, steps, world, ms):
+    """Whole-job throughput: the FLOPs of every replica's steps over the slowest rank's time."""
+    return world * flops_per_replica_step * steps / (ms * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -289,17 +305,14 @@ def run_ours(args):
     if st:
         raise RuntimeError(f"device status after timed steps: {cca.strerror(st)}")
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     pairs = causal_pairs_total(w, chunks)
     flops_fwd = 4 * w.D * pairs
     flops_bwd = 10 * w.D * pairs
     flops_step = flops_fwd + flops_bwd
     ms_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops_step, args.steps, world, total_ms)
 
     def streamed_leg():
         # Chunk-streamed calls, as SPPO and InfiniPipe invoke attention: the forward
@@ -339,7 +352,8 @@ def run_ours(args):
             raise RuntimeError(f"device status after streamed steps: {cca.strerror(st)}")
         s_fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in s_ev)
         s_bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in s_ev)
-        streamed = {"value": world * flops_step / ((s_fwd_ms + s_bwd_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        s_job_ms = max_over_ranks(s_fwd_ms + s_bwd_ms, world, dev)
+        streamed = {"value": job_tflops(flops_step, 1, world, s_job_ms), "unit": "TFLOP/s",
                     "steps": s_steps, "calls_per_step": 2 * len(chunks),
                     "fwd_tflops": flops_fwd / (s_fwd_ms * 1e-3) / 1e12,
                     "bwd_tflops": flops_bwd / (s_bwd_ms * 1e-3) / 1e12,
@@ -414,14 +428,11 @@ def run_ours(args):
         e2e_ms = e0.elapsed_time(e1)
         h2d_ms = sum(h2d_start[i].elapsed_time(h2d_done[i]) for i in range(e2e_steps))
         d2h_ms = sum(d2h_start[i].elapsed_time(d2h_done[i]) for i in range(e2e_steps))
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         nbytes = lambda x: x.numel() * x.element_size()
         h2d = sum(nbytes(x) for x in (q, k, v, do))
         d2h = sum(nbytes(x) for x in (o, lse, dq, dk, dv))
-        e2e_value = world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+        e2e_value = job_tflops(flops_step, e2e_steps, world, e2e_ms)
         return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "copies": "pinned host buffers; upload and read-back streams overlapped with compute",

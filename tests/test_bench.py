@@ -1,6 +1,6 @@
 """Host-side checks of bench.py (no GPU): the oracle arm's JSON line, the
-gating of the committed ncu traffic record by the kernel sources' hash, and
-the workload config keys."""
+gating of the committed ncu traffic record by the kernel sources' hash, the
+workload config keys, and the replicas' timing over gloo with two ranks."""
 import json
 import os
 import subprocess
@@ -86,3 +86,33 @@ def test_reference_arm_under_torchrun_prints_from_rank_0_only():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def _replica_rank(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 100.0 + 50.0 * rank                 # rank 1 is the slow one
+        job_ms = bench.max_over_ranks(ms, world, "cpu")
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"job_ms": job_ms, "tflops": bench.job_tflops(1e12, 4, world, job_ms)}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_report_the_slowest_rank_over_gloo(tmp_path):
+    """N > 1 runs one replica per rank: every rank times the job by the slowest
+    rank, and the whole-job value counts the work of all ranks."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.start_processes(_replica_rank, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    got = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(2)]
+    for g in got:
+        assert g["job_ms"] == 150.0
+        # 2 replicas x 4 steps x 1e12 FLOP in 0.15 s
+        assert abs(g["tflops"] - 2 * 4 * 1.0 / 0.15) < 1e-9
+    assert bench.max_over_ranks(7.0, 1, "cpu") == 7.0
