@@ -154,6 +154,46 @@ def time_oracle_sample(w, tokens, seed):
     return 14 * D * pairs / dt / 1e12, dt
 
 
+def row_kernel_bytes(w, chunks):
+    """Algorithmic HBM bytes per launch of the three row kernels of one step.
+
+    attn_bwd_prep reads O and dO (bf16) and writes D_t (fp32) and the zeroed
+    fp32 dQ accumulator row; attn_bwd_dq reads that accumulator and writes bf16
+    dQ: 4D + 4 + 4D and 4D + 2D bytes per (row, query head). attn_fwd_merge reads
+    (4D + 4) bytes of every key-range partial a re-split row can see and writes
+    its bf16 O and fp32 LSE (2D + 4). The partial rows of a two-part split run
+    from the 128-row tile holding the split point m to the chunk's end; rows
+    before m see the first part only. The merge figure is None for plans with
+    P-part splits (kv_split < 0), whose boundaries only the library computes,
+    and 0 when no chunk is split."""
+    D, rows = w.D, w.B * w.H * w.L
+    merge = 0
+    for qb, qe, cb, m in chunks:
+        if m < 0:
+            merge = None
+            break
+        if m == 0:
+            continue
+        pr0 = qb + 128 * ((m - qb) // 128) if m > qb else qb
+        seen = 2 * (qe - max(pr0, m)) + max(0, m - pr0)
+        merge += w.B * w.H * (seen * (4 * D + 4) + (qe - pr0) * (2 * D + 4))
+    return {"bwd_prep": rows * (8 * D + 4), "bwd_dq": rows * 6 * D, "fwd_merge": merge}
+
+
+def hbm_kernels(w, chunks, stage_ms, peak_gbs):
+    """Achieved GB/s of the HBM-bound row kernels: algorithmic bytes per launch
+    over the launch's mean event time on the launching stream."""
+    out = {}
+    for name, nbytes in row_kernel_bytes(w, chunks).items():
+        if not nbytes or stage_ms[name] <= 0:
+            out[name] = None
+            continue
+        gbs = nbytes / (stage_ms[name] * 1e-3) / 1e9
+        out[name] = {"bytes": nbytes, "ms": stage_ms[name], "achieved": gbs, "peak": peak_gbs,
+                     "unit": "GB/s", "frac": gbs / peak_gbs}
+    return out
+
+
 def workload_flops(w):
     """Algorithmic fwd+bwd FLOPs of a workload: 14 D per visible pair (per document when packed)."""
     return 14 * w.D * causal_pairs_total(w, None)
@@ -468,6 +508,7 @@ def run_ours(args):
                          "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                          "frac_of_burst": achieved / peak_burst, "traffic": measured_traffic(w.name),
                          "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
+            "hbm_kernels": hbm_kernels(w, chunks, stage_ms, peaks["hbm_gbs"]),
             "gpu_launches": launches_per_step * args.steps,
             "e2e": e2e,
             "clocks": clk,

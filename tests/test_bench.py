@@ -116,3 +116,27 @@ def test_replicas_report_the_slowest_rank_over_gloo(tmp_path):
         # 2 replicas x 4 steps x 1e12 FLOP in 0.15 s
         assert abs(g["tflops"] - 2 * 4 * 1.0 / 0.15) < 1e-9
     assert bench.max_over_ranks(7.0, 1, "cpu") == 7.0
+
+
+def test_row_kernel_bytes():
+    """Algorithmic bytes of the HBM-bound row kernels, counted by hand."""
+    import chunked_causal_attention_gb300 as cca
+    from chunked_causal_attention_gb300.workloads import WORKLOADS, Workload
+    w = WORKLOADS["7b_128k"]
+    rows = 32 * 131072
+    got = bench.row_kernel_bytes(w, cca.attn_plan(w.L, w.N, w.mode))
+    assert got["bwd_prep"] == rows * (2 * 256 + 4 + 512)       # O, dO in; D_t and the zeroed accumulator out
+    assert got["bwd_dq"] == rows * (512 + 256)                  # fp32 accumulator in, bf16 dQ out
+    # first chunk [0, 32768) split at 16384, last [126848, 131072) at 129024: every
+    # partial row lies past its split point and reads both parts
+    assert got["fwd_merge"] == 32 * (16384 + 2048) * (2 * (4 * 128 + 4) + 2 * 128 + 4)
+    assert bench.row_kernel_bytes(w, cca.attn_plan_multiplex(w.L, w.N, 3))["fwd_merge"] is None
+    assert bench.row_kernel_bytes(w, cca.attn_plan(w.L, w.N, cca.PLAN_FLOPS))["fwd_merge"] == 0
+    # a split point inside a tile: partial rows from 256, rows 256..299 see the first part only
+    small = Workload("s", 1, 2, 64, 1000)
+    got = bench.row_kernel_bytes(small, [(0, 1000, 0, 300)])
+    assert got["fwd_merge"] == 2 * ((44 + 2 * 700) * (4 * 64 + 4) + 744 * (2 * 64 + 4))
+    hk = bench.hbm_kernels(small, [(0, 1000, 0, 0)], {"bwd_prep": 1.0, "bwd_dq": 0.5, "fwd_merge": 0.01}, 1000.0)
+    assert hk["fwd_merge"] is None
+    assert hk["bwd_prep"]["achieved"] == pytest.approx(2000 * (8 * 64 + 4) / 1e-3 / 1e9)
+    assert hk["bwd_dq"]["frac"] == pytest.approx(2000 * 6 * 64 / 0.5e-3 / 1e9 / 1000.0)
