@@ -1,6 +1,8 @@
 """Host-side checks of bench.py (no GPU): the oracle arm's JSON line, the
 gating of the committed ncu traffic record by the kernel sources' hash, the
-workload config keys, and the replicas' timing over gloo with two ranks."""
+workload config keys, the replicas' timing over gloo with two ranks, the
+row kernels' algorithmic bytes, and the GPU arm's whole JSON line on a fake
+device (torch.cuda and the compute calls replaced by stand-ins)."""
 import json
 import os
 import subprocess
@@ -140,3 +142,86 @@ def test_row_kernel_bytes():
     assert hk["fwd_merge"] is None
     assert hk["bwd_prep"]["achieved"] == pytest.approx(2000 * (8 * 64 + 4) / 1e-3 / 1e9)
     assert hk["bwd_dq"]["frac"] == pytest.approx(2000 * 6 * 64 / 0.5e-3 / 1e9 / 1000.0)
+
+
+class _FakeEvent:
+    """A CUDA event stand-in: every record advances a clock by 1 ms."""
+    clock = [0.0]
+
+    def __init__(self, enable_timing=False):
+        self.t = None
+
+    def record(self, stream=None):
+        _FakeEvent.clock[0] += 1.0
+        self.t = _FakeEvent.clock[0]
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+class _FakeStream:
+    def wait_event(self, event):
+        pass
+
+
+def test_gpu_arm_json_line_with_a_fake_device(monkeypatch, capsys):
+    """The GPU arm's host logic end to end, with torch.cuda, the device and the
+    compute calls replaced by stand-ins (no kernel runs): the JSON line has
+    every key the bench contract asks for, on a small plan with re-split edges."""
+    import contextlib
+
+    import torch
+    import chunked_causal_attention_gb300 as cca
+    from chunked_causal_attention_gb300 import workloads as W
+
+    real_torch = torch
+
+    class TorchProxy(types.ModuleType):
+        def __init__(self):
+            super().__init__("torch")
+            self.cuda = types.SimpleNamespace(
+                set_device=lambda *a: None, Event=_FakeEvent, synchronize=lambda *a: None,
+                current_stream=lambda *a: _FakeStream(), Stream=lambda *a: _FakeStream(),
+                stream=lambda s: contextlib.nullcontext())
+
+        def __getattr__(self, name):
+            return getattr(real_torch, name)
+
+        def device(self, *args, **kwargs):
+            return real_torch.device("cpu")
+
+        def empty(self, *args, pin_memory=False, **kwargs):
+            return real_torch.empty(*args, **kwargs)
+
+    calls = []
+    for name in ("attn_fwd_tiles", "attn_fwd_merge", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_fwd",
+                 "attn_bwd", "attn_bwd_chunk"):
+        monkeypatch.setattr(cca, name, lambda *a, _n=name: calls.append(_n))
+    monkeypatch.setattr(cca, "attn_status", lambda *a: 0)
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)
+    monkeypatch.setitem(sys.modules, "torch", TorchProxy())
+    monkeypatch.setitem(W.WORKLOADS, "mini_resplit",
+                        W.Workload("mini_resplit", 1, 2, 64, 2048, N=4, mode=W.PLAN_FLOPS_RESPLIT_EDGES, seed=5))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "2", "--warmup", "3", "--workload", "mini_resplit",
+                                      "--cpu-sample-tokens", "256"])
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks",
+                "hbm_kernels", "streamed"):
+        assert key in d, key
+    assert d["metric"] == bench.METRIC and d["n_gpus"] == 1 and d["steps"] == 2 and d["value"] > 0
+    assert d["config"]["workload"] == "mini_resplit"
+    assert d["roofline"]["bound"] == "tensor" and 0 < d["roofline"]["frac"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 4 * 2 * 2048 * 64 * 2
+    assert d["e2e"]["d2h_bytes_per_step"] == 4 * 2 * 2048 * 64 * 2 + 2 * 2048 * 4
+    assert d["hbm_kernels"]["fwd_merge"]["bytes"] > 0 and d["hbm_kernels"]["bwd_prep"]["frac"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
+    assert d["gpu_launches"] == 5 * 2
+    # one step = the five stage calls; warm-up and timed steps, then the streamed and e2e legs
+    assert calls[:5] == ["attn_fwd_tiles", "attn_fwd_merge", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq"]
+    assert calls.count("attn_bwd_tiles") == 3 + 2
