@@ -14,47 +14,112 @@
 namespace attn {
 namespace {
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
 // One warp per (segment row, batch*head): merge the row's partials. Lane l
 // takes the four elements from d = 4l (D is a multiple of 8, at most 128).
-__global__ void __launch_bounds__(256) merge_kernel(MergeArgs a) {
+// The row's loads go out in few dependent rounds: the parts it sees (a
+// prefix of the segment's increasing key boundaries) are counted by one
+// ballot; then lane p reads part p's LSE while every lane reads its slice of
+// the first two parts' O; the weights reach all lanes by shuffles.
+__global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (w >= a.total_work) return;
+    if (w >= a.total_work) return;   // the same w for every lane of a warp
     const int D = a.g.D;
     int si = 0;
     while (si + 1 < a.n_segs && a.segs[si + 1].work0 <= w) ++si;
     const MergeSeg sg = a.segs[si];
     const int BH = a.g.B * a.g.H;
     const int64_t local = w - sg.work0;
-    const int bh = (int)(local / sg.R);
-    const int i = (int)(local % sg.R);
+    int bh, i;
+    if (local <= INT32_MAX) {
+        const uint32_t l = (uint32_t)local, r = (uint32_t)sg.R;
+        bh = (int)(l / r);
+        i = (int)(l - (uint32_t)bh * r);
+    } else {
+        bh = (int)(local / sg.R);
+        i = (int)(local % sg.R);
+    }
     const int t = sg.row0 + i;
     const int64_t R = sg.R;
+    const int64_t blk = sg.blk;
     const int32_t* kb = a.kbounds + sg.kb;
-    // parts whose key range starts at or before this row
+    // parts whose key range starts at or before this row (at least part 0,
+    // which starts at the document start)
     int np = 0;
-    while (np < sg.P && kb[np] <= t) ++np;
-    float mx = -INFINITY;
-    for (int p = 0; p < np; ++p) mx = fmaxf(mx, a.ws_f[sg.off0 + p * sg.blk + (int64_t)BH * R * D + (int64_t)bh * R + i]);
+    for (int p0 = 0; p0 < sg.P; p0 += 32) {
+        const int p = p0 + lane;
+        np += __popc(__ballot_sync(0xffffffffu, p < sg.P && kb[p] <= t));
+    }
+    // part p's LSE is at lse_row[p * blk], its O row at o_row[p * blk]
+    const float* lse_row = a.ws_f + sg.off0 + (int64_t)BH * R * D + (int64_t)bh * R + i;
+    const float* o_row = a.ws_f + sg.off0 + ((int64_t)bh * R + i) * D;
     const int d = 4 * lane;
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (mx != -INFINITY) {
-        float tot = 0.f;
-        for (int p = 0; p < np; ++p) {
-            const float* base = a.ws_f + sg.off0 + p * sg.blk;
-            const float lp = base[(int64_t)BH * R * D + (int64_t)bh * R + i];
-            if (lp == -INFINITY) continue;
-            const float ep = __expf(lp - mx);
-            tot += ep;
-            if (d < D) {
-                const float4 v = *reinterpret_cast<const float4*>(base + ((int64_t)bh * R + i) * D + d);
-                r.x = fmaf(ep, v.x, r.x);
-                r.y = fmaf(ep, v.y, r.y);
-                r.z = fmaf(ep, v.z, r.z);
-                r.w = fmaf(ep, v.w, r.w);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v0 = zero, v1 = zero;
+    if (d < D) {
+        v0 = *reinterpret_cast<const float4*>(o_row + d);
+        if (np > 1) v1 = *reinterpret_cast<const float4*>(o_row + blk + d);
+    }
+    float4 r = zero;
+    float tot = 0.f, mx;
+    if (np <= 2) {
+        // two parts at most (every split of one point): lanes 0 and 1 read the LSEs
+        const float l = lane < np ? lse_row[lane * blk] : -INFINITY;
+        const float l0 = __shfl_sync(0xffffffffu, l, 0), l1 = __shfl_sync(0xffffffffu, l, 1);
+        mx = fmaxf(l0, l1);
+        if (mx != -INFINITY) {
+            if (l0 != -INFINITY) {
+                const float e = __expf(l0 - mx);
+                tot += e;
+                r = make_float4(fmaf(e, v0.x, r.x), fmaf(e, v0.y, r.y), fmaf(e, v0.z, r.z), fmaf(e, v0.w, r.w));
+            }
+            if (l1 != -INFINITY) {
+                const float e = __expf(l1 - mx);
+                tot += e;
+                r = make_float4(fmaf(e, v1.x, r.x), fmaf(e, v1.y, r.y), fmaf(e, v1.z, r.z), fmaf(e, v1.w, r.w));
             }
         }
+    } else {
+        // P-part splits: lane p reads part p's LSE, 32 parts at a time
+        mx = -INFINITY;
+        for (int p0 = 0; p0 < np; p0 += 32) {
+            const int p = p0 + lane;
+            if (p < np) mx = fmaxf(mx, lse_row[p * blk]);
+        }
+        mx = warp_max(mx);
+        for (int p0 = 0; p0 < np && mx != -INFINITY; p0 += 32) {
+            const int p = p0 + lane;
+            float e = 0.f;
+            if (p < np) {
+                const float lp = lse_row[p * blk];
+                if (lp != -INFINITY) e = __expf(lp - mx);
+            }
+            tot += warp_sum(e);
+            const int cnt = min(32, np - p0);
+            for (int j = 0; j < cnt; ++j) {
+                const float ej = __shfl_sync(0xffffffffu, e, j);
+                const int pj = p0 + j;
+                float4 v = pj == 0 ? v0 : v1;
+                if (pj > 1 && d < D) v = *reinterpret_cast<const float4*>(o_row + pj * blk + d);
+                if (ej != 0.f)
+                    r = make_float4(fmaf(ej, v.x, r.x), fmaf(ej, v.y, r.y), fmaf(ej, v.z, r.z), fmaf(ej, v.w, r.w));
+            }
+        }
+    }
+    float lse = -INFINITY;
+    if (mx != -INFINITY) {
         lse = mx + __logf(tot);
         const float inv = 1.f / tot;
         r.x *= inv;
