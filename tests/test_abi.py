@@ -346,7 +346,8 @@ def test_compute_wrappers_reject_cpu_and_mismatched_tensors():
 def test_header_is_plain_c(tmp_path):
     """include/attn.h is a C header: a C99 program that includes it, links
     libattn.so and calls the host-only entry points (planner, workspace size,
-    error strings, version) compiles and gives the same plan as the binding."""
+    error strings, version) compiles and gives the same plan as the binding;
+    its compute calls without buffers return ATTN_E_INVAL from the host."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
@@ -364,6 +365,10 @@ int main(void) {
     attn_shape s = {1, 32, 131072, 128, 32LL * 131072 * 128, 128, 131072LL * 128, 0.08838834764831845f, 0, 0, 0, 0};
     size_t bytes = 0;
     if (attn_workspace_size(&s, c, n, 1, &bytes) != ATTN_OK || bytes == 0) return 2;
+    /* compute calls with missing buffers are refused on the host, before any CUDA call */
+    if (attn_fwd(NULL, NULL, NULL, c, n, &s, NULL, NULL, NULL, 0, NULL) != ATTN_E_INVAL) return 4;
+    if (attn_bwd(NULL, NULL, NULL, NULL, NULL, NULL, c, n, &s, NULL, NULL, NULL, NULL, 0, NULL) != ATTN_E_INVAL)
+        return 5;
     s.D = 100;
     if (attn_workspace_size(&s, c, n, 1, &bytes) != ATTN_E_UNSUPPORTED) return 3;
     printf("%d", (int)n);
