@@ -134,9 +134,24 @@ def fit_calls():
     return calls
 
 
-def fit():
+def fit_constants(rows, ms):
+    """(alpha1, alpha2, beta1) >= 0 minimising the squared relative error of
+    alpha1 quad + alpha2 tokens + beta1 against the measured times ``ms``
+    (rows: [quad, tokens, 1] per call), and the relative errors per call."""
     import numpy as np
     from scipy.optimize import nnls
+    A = np.array(rows, dtype=np.float64)
+    y = np.array(ms, dtype=np.float64)
+    W = A / y[:, None]                         # relative residuals: (pred - y) / y
+    scale = W.max(axis=0)
+    x, _ = nnls(W / scale, np.ones_like(y))
+    a1, a2, b1 = (x / scale).tolist()
+    pred = A @ np.array([a1, a2, b1])
+    return a1, a2, b1, np.abs(pred - y) / y
+
+
+def fit():
+    import numpy as np
     calls = fit_calls()
     r = Runner([calls])
     rows, ms, fw_ms, bw_ms = [], [], [], []
@@ -147,14 +162,7 @@ def fit():
         ms.append(f + b)
         fw_ms.append(f)
         bw_ms.append(b)
-    A = np.array(rows, dtype=np.float64)
-    y = np.array(ms, dtype=np.float64)
-    W = A / y[:, None]                         # relative residuals: (pred - y) / y
-    scale = W.max(axis=0)
-    x, _ = nnls(W / scale, np.ones_like(y))
-    a1, a2, b1 = (x / scale).tolist()
-    pred = A @ np.array([a1, a2, b1])
-    rel = np.abs(pred - y) / y
+    a1, a2, b1, rel = fit_constants(rows, ms)
     out = {"alpha1_ms": a1, "alpha2_ms": a2, "beta1_ms": b1, "unit": "ms per call (forward + backward)",
            "shape": f"H{H} D{D} bf16", "calls": len(calls), "max_rel_err": float(rel.max()),
            "median_rel_err": float(np.median(rel)),
