@@ -486,6 +486,8 @@ def run_ours(args):
     e2e = skipped if args.device_only else e2e_leg()
 
     peaks, peak_src = load_peaks()
+    fwd_tflops = flops_fwd / ((stage_ms["fwd_tiles"] + stage_ms["fwd_merge"]) * 1e-3) / 1e12
+    bwd_tflops = flops_bwd / ((stage_ms["bwd_prep"] + stage_ms["bwd_tiles"] + stage_ms["bwd_dq"]) * 1e-3) / 1e12
     dom = "bwd_tiles"
     dom_ms = stage_ms[dom]
     achieved = flops_bwd / (dom_ms * 1e-3) / 1e12
@@ -498,10 +500,10 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, args),
             "pct_of_peak": {"burst": 100 * value / world / peak_burst, "sustained": 100 * value / world / peak_sus,
+                            "fwd_burst": 100 * fwd_tflops / peak_burst, "bwd_burst": 100 * bwd_tflops / peak_burst,
                             "peak_source": peak_src},
-            "fwd_tflops": flops_fwd / ((stage_ms["fwd_tiles"] + stage_ms["fwd_merge"]) * 1e-3) / 1e12,
-            "bwd_tflops": flops_bwd / ((stage_ms["bwd_prep"] + stage_ms["bwd_tiles"] + stage_ms["bwd_dq"]) * 1e-3)
-                          / 1e12,
+            "fwd_tflops": fwd_tflops,
+            "bwd_tflops": bwd_tflops,
             "stage_ms": stage_ms,
             "roofline": {"kernel": "bwd key-tile kernel (attn_bwd_tiles)", "bound": "tensor",
                          "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,

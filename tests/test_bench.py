@@ -222,6 +222,8 @@ def test_gpu_arm_json_line_with_a_fake_device(monkeypatch, capsys):
     assert d["hbm_kernels"]["fwd_merge"]["bytes"] > 0 and d["hbm_kernels"]["bwd_prep"]["frac"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["gpu_launches"] == 5 * 2
+    for key in ("burst", "sustained", "fwd_burst", "bwd_burst"):
+        assert d["pct_of_peak"][key] > 0
     # one step = the five stage calls; warm-up and timed steps, then the streamed and e2e legs
     assert calls[:5] == ["attn_fwd_tiles", "attn_fwd_merge", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq"]
     assert calls.count("attn_bwd_tiles") == 3 + 2
