@@ -96,6 +96,7 @@ struct FwdLayout {
     std::vector<int32_t> kbounds;   // key-range boundaries of the segments
     size_t off_items, off_segs, off_kb, off_parts, bytes;
     int64_t merge_work;
+    int64_t part_floats;            // floats of the partial region
 };
 
 void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
@@ -147,6 +148,7 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
     L.off_kb = L.off_segs + round_up(L.segs.size() * sizeof(MergeSeg), kAlign);
     L.off_parts = L.off_kb + round_up(L.kbounds.size() * sizeof(int32_t), kAlign);
     L.bytes = L.off_parts + round_up((size_t)part_floats * sizeof(float), kAlign);
+    L.part_floats = part_floats;
 }
 
 // --------------------------------------------------------------- backward layout
@@ -231,6 +233,11 @@ void attn::wait_settings(uint64_t* wait_ns, int32_t* stall) {
     if (const char* e = std::getenv("ATTN_TEST_STALL_PRODUCER")) *stall = std::atoi(e) != 0;
 }
 
+bool attn::test_inconsistent_item() {
+    const char* e = std::getenv("ATTN_TEST_INCONSISTENT_ITEM");
+    return e && std::atoi(e) != 0;
+}
+
 namespace {
 
 int upload(void* dst, const void* src, size_t bytes, cudaStream_t s) {
@@ -277,9 +284,12 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
     if (do_tiles) {
         if ((st = reset_header(ws, s))) return st;
         if (!L.items.empty()) {
+            // index-check test only: an empty row range, which addresses nothing
+            if (test_inconsistent_item()) L.items[0].r1 = L.items[0].r0;
             if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(FwdItem), s))) return st;
             FwdArgs a;
             a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.ws_f = ws_f;
+            a.part_floats = L.part_floats;
             a.status = (uint32_t*)ws;
             a.items = (const FwdItem*)(w + L.off_items);
             a.n_items = (int32_t)L.items.size();
@@ -294,8 +304,11 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
         if ((st = upload(w + L.off_kb, L.kbounds.data(), L.kbounds.size() * sizeof(int32_t), s))) return st;
         MergeArgs a;
         a.o = o; a.lse = lse; a.ws_f = ws_f;
+        a.part_floats = L.part_floats;
         a.segs = (const MergeSeg*)(w + L.off_segs);
         a.kbounds = (const int32_t*)(w + L.off_kb);
+        a.n_kbounds = (int32_t)L.kbounds.size();
+        a.status = (uint32_t*)ws;
         a.n_segs = (int32_t)L.segs.size();
         a.total_work = L.merge_work;
         a.g = g;
@@ -322,11 +335,18 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
     }
     if (stages & kPrep) {
         if ((st = reset_header(ws, s))) return st;
-        PrepArgs a{o, dout, delta, dq_acc, segs, n_segs, L.rows, g};
+        PrepArgs a{o, dout, delta, dq_acc, segs, n_segs, L.rows, (uint32_t*)ws, g};
         if ((st = launched(launch_bwd_prep(a, s)))) return st;
     }
     if (stages & kTiles) {
-        if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) return st;
+        if (test_inconsistent_item() && !L.items.empty()) {
+            // index-check test only: an empty query range, which addresses nothing
+            std::vector<BwdItem> items = L.items;
+            items[0].q_end = items[0].q_lo;
+            if ((st = upload(w + L.off_items, items.data(), items.size() * sizeof(BwdItem), s))) return st;
+        } else if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) {
+            return st;
+        }
         BwdArgs a;
         a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
         a.dk = dk; a.dv = dv; a.dq_acc = dq_acc;
@@ -341,7 +361,7 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
         if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
     }
     if (stages & kDq) {
-        DqArgs a{dq_acc, dq, segs, n_segs, L.rows, g};
+        DqArgs a{dq_acc, dq, segs, n_segs, L.rows, (uint32_t*)ws, g};
         if ((st = launched(launch_bwd_dq(a, s)))) return st;
     }
     return ATTN_OK;

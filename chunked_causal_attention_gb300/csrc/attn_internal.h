@@ -90,6 +90,7 @@ struct FwdArgs {
     const void* q; const void* k; const void* v;
     void* o; float* lse;
     float* ws_f;
+    int64_t part_floats;  // floats of the partial region at ws_f (index checks)
     uint32_t* status;
     const FwdItem* items;
     int32_t n_items;
@@ -102,8 +103,11 @@ struct FwdArgs {
 struct MergeArgs {
     void* o; float* lse;
     const float* ws_f;
+    int64_t part_floats;      // floats of the partial region at ws_f (index checks)
     const MergeSeg* segs;
     const int32_t* kbounds;   // key-range boundaries of all segments
+    int32_t n_kbounds;
+    uint32_t* status;
     int32_t n_segs;
     int64_t total_work;   // sum over segments of R * B * H
     Geom g;
@@ -116,6 +120,7 @@ struct PrepArgs {
     float* delta; float* dq_acc;
     const RowSeg* segs; int32_t n_segs;
     int32_t rows;
+    uint32_t* status;
     Geom g;
 };
 
@@ -142,12 +147,18 @@ struct BwdArgs {
 // ATTN_WAIT_LIMIT_MS (default 4000) and ATTN_TEST_STALL_PRODUCER (default 0,
 // used by the failure-detection test to make every wait run out).
 void wait_settings(uint64_t* wait_ns, int32_t* stall);
+// ATTN_TEST_INCONSISTENT_ITEM (default 0): used by the index-check test. The
+// first work item of each tile kernel is made inconsistent before it is copied
+// to the workspace, in a way that addresses nothing outside the buffers (an
+// empty query range), so that the kernels' descriptor checks must report it.
+bool test_inconsistent_item();
 
 struct DqArgs {
     const float* dq_acc;  // rows as PrepArgs
     void* dq;
     const RowSeg* segs; int32_t n_segs;
     int32_t rows;
+    uint32_t* status;
     Geom g;
 };
 

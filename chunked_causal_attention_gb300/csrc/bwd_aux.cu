@@ -4,7 +4,8 @@
 //   dq:   dQ = bf16(fp32 accumulator), written with the caller's strides.
 // One warp per (batch*head, workspace row); the rows are the tokens of one or
 // more segments (all tokens for the whole backward, the chunks' rows for the
-// chunk-streamed backward).
+// chunk-streamed backward). A row whose segment maps it outside the tokens is
+// reported as ATTN_E_BOUNDS and not touched.
 #include "device_common.cuh"
 
 namespace attn {
@@ -34,6 +35,10 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
     if (w >= total) return;
     const int D = a.g.D;
     const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
+    if (t < 0 || t >= a.g.T) {                 // a row segment outside the tokens
+        if (lane == 0) set_error(a.status, ATTN_E_BOUNDS);
+        return;
+    }
     const int b = bh / a.g.H, h = bh % a.g.H;
     const int64_t off = (int64_t)b * a.g.sb + (int64_t)h * a.g.sh + (int64_t)t * a.g.st;
     const int d = 4 * lane;
@@ -62,6 +67,10 @@ __global__ void __launch_bounds__(256) dq_kernel(DqArgs a) {
     const int d = 4 * lane;
     if (d >= D) return;
     const int bh = (int)(w / a.rows), t = token_of_row(a.segs, a.n_segs, (int)(w % a.rows));
+    if (t < 0 || t >= a.g.T) {                 // a row segment outside the tokens
+        if (lane == 0) set_error(a.status, ATTN_E_BOUNDS);
+        return;
+    }
     const int b = bh / a.g.H, h = bh % a.g.H;
     const float4 v = *reinterpret_cast<const float4*>(a.dq_acc + w * D + d);
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +

@@ -41,7 +41,12 @@
 //                fp32 tile is exactly its size), then one thread issues TMA
 //                reduce-adds into the fp32 accumulator and hands the stage back
 //                to the producer once the TMA engine has read it.
-// Every mbarrier wait is bounded (ATTN_E_TIMEOUT in the status word).
+// Every mbarrier wait is bounded (ATTN_E_TIMEOUT in the status word). The
+// warps of a group that meets at named barriers leave their loop only
+// together, by a vote taken at one of those barriers (bar.red), so a wait
+// that gives up in one warp cannot leave the others waiting for it. Every
+// role checks each work item against the geometry before using it
+// (ATTN_E_BOUNDS; all roles read the same item and decide alike).
 #include "tc_common.cuh"
 
 namespace attn {
@@ -238,6 +243,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 int32_t it, bkv;
                 decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
+                if (!bwd_item_ok(item, a.g.T, a.rows)) {
+                    set_error(a.status, ATTN_E_BOUNDS);
+                    *abort_flag = 1;
+                    break;
+                }
                 const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
                 ok = mbar_wait(bar(LY::B_KVEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -271,6 +281,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 int32_t it, bkv;
                 decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
+                if (!bwd_item_ok(item, a.g.T, a.rows)) {
+                    set_error(a.status, ATTN_E_BOUNDS);
+                    *abort_flag = 1;
+                    break;
+                }
                 const int nq = (item.q_end - item.q_lo + 127) / 128;
                 ok = mbar_wait(bar(LY::B_KVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -347,10 +362,19 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         // query 64*grp + (krow & 63), fetched one block ahead
         const bool stage_l = krow < 64;
         float* stage_dst = (stage_l ? s_nl : s_nd) + 64 * grp + (krow & 63);
-        for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+        // The two groups synchronise on named barriers, so a thread never leaves
+        // the loop on its own: `ok` changes only through a group vote
+        // (named_sync_all), which every thread of the group reaches, and the item
+        // check gives the same answer in every thread.
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++ic) {
             int32_t it, bkv;
             decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];
+            if (!bwd_item_ok(item, a.g.T, a.rows)) {
+                set_error(a.status, ATTN_E_BOUNDS);
+                *abort_flag = 1;
+                break;
+            }
             const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
             const int key = item.j0 + krow;
@@ -373,11 +397,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             int i = 0, g = 0;                              // the block: query head hk*G + g, i-th from the top
             for (int blk = 0; blk < G * nq; ++blk, ++gb) {
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;  // query blocks walked from the last one down
-                if (*abort_flag) {
+                // the first of the block's two barriers carries the group's vote: go on
+                // only if every wait of the previous block succeeded in every thread and
+                // no thread has seen the abort flag
+                if (!named_sync_all(1 + grp, 128, ok && !*abort_flag)) {
                     ok = false;
                     break;
                 }
-                named_sync(1 + grp, 128);
                 *stage_dst = next * mul;
                 named_sync(1 + grp, 128);
                 if (i + 1 < nq) {
@@ -387,31 +413,37 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     const int q = item.q_lo + (nq - 1) * 128 + qoff;
                     next = q < item.q_end ? src[q] : 0.f;
                 }
-                ok = mbar_wait(bar(LY::B_SDP), gb & 1, abort_flag, a.status, a.wait_ns);
-                if (!ok) break;
-                if (gb > 0) {
-                    // dS in shared memory is free once dQ of the previous block has completed
-                    ok = mbar_wait(bar(LY::B_DQFULL), (gb - 1) & 1, abort_flag, a.status, a.wait_ns);
-                    if (!ok) break;
+                // a failed wait skips the block's work (the warp-collective TMEM loads
+                // and stores run in all lanes of a warp or in none); the group leaves at
+                // the next vote
+                ok = mbar_wait_warp(bar(LY::B_SDP), gb & 1, abort_flag, a.status, a.wait_ns);
+                // dS in shared memory is free once dQ of the previous block has completed
+                if (ok && gb > 0) ok = mbar_wait_warp(bar(LY::B_DQFULL), (gb - 1) & 1, abort_flag, a.status, a.wait_ns);
+                if (ok) {
+                    tc_fence_after();
+                    // masks are needed where some key of the tile lies after some query of
+                    // the block, where the block runs past the document or chunk end, and
+                    // on a partial key tile
+                    const bool edge = (i0 < item.j1 - 1) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
+                    if (edge)
+                        sg_block<true>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2,
+                                       bar(LY::B_PCH));
+                    else
+                        sg_block<false>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2,
+                                        bar(LY::B_PCH));
                 }
-                tc_fence_after();
-                // masks are needed where some key of the tile lies after some query of the
-                // block, where the block runs past the document or chunk end, and on a
-                // partial key tile
-                const bool edge = (i0 < item.j1 - 1) || (i0 + 128 > item.q_end) || (item.j1 - item.j0 < 128);
-                if (edge)
-                    sg_block<true>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
-                else
-                    sg_block<false>(tmem + lane_addr, grp, krow, key, i0, item, s_nl, s_nd, ds_row, sl2x2, bar(LY::B_PCH));
                 if (++i == nq) {
                     i = 0;
                     ++g;
                 }
             }
-            if (!ok) break;
-            // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16)
-            ok = mbar_wait(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
-            if (!ok) break;
+            // epilogue: warps 4-7 write dK * scale, warps 8-11 write dV (bf16); the
+            // group enters it only together (the streamed epilogue has barriers)
+            if (ok) ok = mbar_wait_warp(bar(LY::B_DKDVFULL), ic & 1, abort_flag, a.status, a.wait_ns);
+            if (!named_sync_all(1 + grp, 128, ok && !*abort_flag)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const int64_t roff = (int64_t)b * a.g.sb_kv + (int64_t)hk * a.g.sh_kv + (int64_t)key * a.g.st_kv;
             const bool live = key < item.j1;
@@ -510,10 +542,17 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         const float sc = a.g.scale;
         uint32_t gb = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x) {
+        // as in the softmax-gradient groups, the four warps leave only together,
+        // by the vote at their barrier (`ok` is the same in every thread)
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
             int32_t it, bkv;
             decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];
+            if (!bwd_item_ok(item, a.g.T, a.rows)) {
+                set_error(a.status, ATTN_E_BOUNDS);
+                *abort_flag = 1;
+                break;
+            }
             const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
             const int nq = (item.q_end - item.q_lo + 127) / 128;
             int i = 0, bhq = b * a.g.H + hk * G;             // the block's index and query head (dQ rows)
@@ -521,35 +560,35 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 const int i0 = item.q_lo + (nq - 1 - i) * 128;
                 const uint32_t s = gb & 1;                   // the stage this block's Q/dO used
                 uint8_t* stage = sm + LY::QDO_OFF + s * LY::STAGE;
-                ok = mbar_wait(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32
-                // columns), one sub-tile at a time; the TMEM columns are released after
-                // the last load
+                ok = mbar_wait_warp(bar(LY::B_DQFULL), gb & 1, abort_flag, a.status, a.wait_ns);
+                if (ok) {
+                    tc_fence_after();
+                    // TMEM -> registers -> staging (fp32, 128-byte swizzled sub-tiles of 32
+                    // columns), one sub-tile at a time; the TMEM columns are released after
+                    // the last load
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + kColDP + cc * 32, r);
-                    tmem_ld_wait();
-                    if (cc == D / 32 - 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar(LY::B_DQFREE));      // TMEM columns free for the next dP^T
-                    }
-                    uint8_t* sub = stage + cc * 16384 + qrow * 128;
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_addr + kColDP + cc * 32, r);
+                        tmem_ld_wait();
+                        if (cc == D / 32 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(bar(LY::B_DQFREE));      // TMEM columns free for the next dP^T
+                        }
+                        uint8_t* sub = stage + cc * 16384 + qrow * 128;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        float4 v = make_float4(__uint_as_float(r[4 * u]) * sc, __uint_as_float(r[4 * u + 1]) * sc,
-                                               __uint_as_float(r[4 * u + 2]) * sc, __uint_as_float(r[4 * u + 3]) * sc);
-                        *reinterpret_cast<float4*>(sub + ((u ^ (qrow & 7)) << 4)) = v;
+                        for (int u = 0; u < 8; ++u) {
+                            float4 v = make_float4(__uint_as_float(r[4 * u]) * sc, __uint_as_float(r[4 * u + 1]) * sc,
+                                                   __uint_as_float(r[4 * u + 2]) * sc, __uint_as_float(r[4 * u + 3]) * sc);
+                            *reinterpret_cast<float4*>(sub + ((u ^ (qrow & 7)) << 4)) = v;
+                        }
                     }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
-                if (*abort_flag) {
+                if (!named_sync_all(3, 128, ok && !*abort_flag)) {
                     ok = false;
                     break;
                 }
-                named_sync(3, 128);
                 if (qrow == 0) {
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
                     // 32-column boxes that start past the head dim hold only the zero

@@ -26,7 +26,11 @@
 //
 // TMEM columns: S buffers at [0,128) and [128,256), O at [256, 256+D).
 // Every mbarrier wait is bounded; a wait that gives up sets ATTN_E_TIMEOUT in
-// the workspace status word and all roles leave their loops.
+// the workspace status word and all roles leave their loops. The softmax
+// warps take each wait's result for the whole warp (its TMEM loads and stores
+// are warp-collective) and meet no named barrier, so each warp leaves on its
+// own. Every role checks each work item against the geometry and the partial
+// region before using it (ATTN_E_BOUNDS).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -135,6 +139,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
+                if (!fwd_item_ok(item, a.g.T, BH, a.g.D, a.part_floats)) {
+                    set_error(a.status, ATTN_E_BOUNDS);
+                    *abort_flag = 1;
+                    break;
+                }
                 const int b = bh / a.g.H, h = bh % a.g.H;
                 const int hk = h / (a.g.H / a.g.Hkv);
                 if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns)) break;
@@ -170,6 +179,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
+                if (!fwd_item_ok(item, a.g.T, BH, a.g.D, a.part_floats)) {
+                    set_error(a.status, ATTN_E_BOUNDS);
+                    *abort_flag = 1;
+                    break;
+                }
                 const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
                 ok = mbar_wait(bar(LY::B_QFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -236,12 +250,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int32_t it, bh;
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const FwdItem item = a.items[it];
+            if (!fwd_item_ok(item, a.g.T, BH, a.g.D, a.part_floats)) {
+                set_error(a.status, ATTN_E_BOUNDS);
+                *abort_flag = 1;
+                break;
+            }
             const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
             const int t_row = item.r0 + row;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nblk && ok; ++j) {
                 const uint32_t t = gt + j, b = t & 1;
-                ok = mbar_wait(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, a.wait_ns);
+                ok = mbar_wait_warp(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_addr + kColS + b * 128;
@@ -305,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // tcgen05.ld/st are warp-collective: rescale O if any row of the warp needs it
                 if (__any_sync(0xffffffffu, rescale) && j > 0) {
                     // O holds the sum over tiles < j once PV_{j-1} has completed
-                    ok = mbar_wait(bar(LY::B_ODONE), (t - 1) & 1, abort_flag, a.status, a.wait_ns);
+                    ok = mbar_wait_warp(bar(LY::B_ODONE), (t - 1) & 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t oa = tmem + lane_addr + kColO;
@@ -327,7 +346,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // epilogue: wait for the last PV of the item, then O / l. This uses the
             // once-per-item barrier: when the softmax warps get here up to two PVs
             // may still be in flight, more than a per-PV parity wait can tell apart.
-            ok = mbar_wait(bar(LY::B_OFULL), ic & 1, abort_flag, a.status, a.wait_ns);
+            ok = mbar_wait_warp(bar(LY::B_OFULL), ic & 1, abort_flag, a.status, a.wait_ns);
             if (!ok) break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

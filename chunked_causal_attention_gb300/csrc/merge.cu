@@ -9,6 +9,8 @@
 // where a part with no visible key (LSE = -inf, or a part that starts after
 // the row) has weight 0.
 // One warp per (segment row, batch*head); fp32 partials in, bf16 O and fp32 LSE out.
+// A segment that does not fit the geometry or the workspace is reported as
+// ATTN_E_BOUNDS and not read.
 #include "device_common.cuh"
 
 namespace attn {
@@ -42,6 +44,13 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
     const MergeSeg sg = a.segs[si];
     const int BH = a.g.B * a.g.H;
     const int64_t local = w - sg.work0;
+    // index checks of the segment before any address is formed from it
+    if (!(sg.R > 0 && sg.row0 >= 0 && (int64_t)sg.row0 + sg.R <= a.g.T && sg.P >= 1 && sg.P <= 64 && sg.kb >= 0 &&
+          sg.kb + sg.P + 1 <= a.n_kbounds && local >= 0 && local < (int64_t)sg.R * BH && sg.off0 >= 0 &&
+          sg.blk >= (int64_t)BH * sg.R * (D + 1) && sg.off0 + sg.P * sg.blk <= a.part_floats)) {
+        if (lane == 0) set_error(a.status, ATTN_E_BOUNDS);
+        return;
+    }
     int bh, i;
     if (local <= INT32_MAX) {
         const uint32_t l = (uint32_t)local, r = (uint32_t)sg.R;

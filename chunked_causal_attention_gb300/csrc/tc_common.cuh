@@ -55,6 +55,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// mbar_wait for a whole warp: the warp goes on only if every lane's wait
+// succeeded, so the warp-collective tcgen05 loads and stores that follow are
+// executed by all of its lanes or by none.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                               uint64_t limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status, limit_ns));
+}
+
+// Named barrier over `n` threads that also returns the AND of their
+// predicates: every thread gets the same answer, so a group that must leave a
+// loop together decides it here.
+__device__ __forceinline__ bool named_sync_all(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
