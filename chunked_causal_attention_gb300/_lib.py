@@ -27,7 +27,8 @@ PLAN_FLOPS_RESPLIT_EDGES = 2
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_plan_multiplex", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
-           "attn_bwd_chunk", "attn_fwd_noalloc", "attn_status", "attn_strerror", "attn_version")
+           "attn_bwd_chunk", "attn_fwd_noalloc", "attn_noalloc_status", "attn_status", "attn_strerror",
+           "attn_version")
 
 # attn_workspace_size passes
 PASS_FWD = 0
@@ -83,6 +84,7 @@ _SIG = {
     "attn_bwd_chunk": ([_VP, _VP, _VP, _VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t,
                         _VP], ctypes.c_int),
     "attn_fwd_noalloc": ([_VP, _VP, _VP, _CP, _I32, _SP, _VP, _VP, _VP], ctypes.c_int),
+    "attn_noalloc_status": ([_VP], ctypes.c_int),
     "attn_status": ([_VP, _VP], ctypes.c_int),
     "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "attn_version": ([], ctypes.c_char_p),
@@ -353,3 +355,8 @@ def attn_fwd_noalloc(q, k, v, chunks, shape, o, lse, stream=None) -> None:
 
 def attn_status(ws, stream=None) -> int:
     return lib().attn_status(_ptr(ws), _stream(stream))
+
+
+def attn_noalloc_status(stream=None) -> int:
+    """Device error word of attn_fwd_noalloc (synchronises the stream; read clears it)."""
+    return lib().attn_noalloc_status(_stream(stream))

@@ -10,37 +10,26 @@
 // passes the inputs and outputs.
 //
 // In host code the array's name is only a host-side stand-in, so its device
-// address is looked up with cudaGetSymbolAddress, once per device, with that
-// device current, the first time the entry point runs there; that first call
-// should therefore come before any stream capture. All calls share the one
-// array and it keeps whatever the last call left in it: the forward clears its
-// status header and rewrites its work list and partials on every call, and
-// calls whose work overlaps on the GPU (different streams, or threads racing
-// on the same device) race on the array.
-#include <mutex>
-
+// address is looked up with cudaGetSymbolAddress in the context that is
+// current when the call runs. The lookup is made on every call and nothing is
+// cached: an address kept from an earlier call would be stale after a device
+// reset or under another context of the same device. The first call in a
+// context loads this library's kernels there, so make it before any stream
+// capture. All calls share the one array and it keeps whatever the last call
+// left in it: the forward clears its status header and rewrites its work list
+// and partials on every call, and calls whose work overlaps on the GPU
+// (different streams, or threads racing on the same device) race on the array.
 #include "attn_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_dev[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device (looked up once per device).
+// Device address of g_scratch in the current context.
 int scratch_address(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_E_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_E_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_dev[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return ATTN_E_CUDA;
-        g_scratch_dev[dev] = p;
-    }
-    *out = g_scratch_dev[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return ATTN_E_CUDA;
+    *out = p;
     return ATTN_OK;
 }
 
@@ -55,4 +44,11 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, con
     void* ws = nullptr;
     if ((st = scratch_address(&ws))) return st;
     return attn_fwd(q, k, v, chunks, n, shape, o, lse, ws, (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int attn_noalloc_status(void* stream) {
+    void* ws = nullptr;
+    int st = scratch_address(&ws);
+    if (st) return st;
+    return attn_status(ws, stream);
 }

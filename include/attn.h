@@ -51,9 +51,12 @@
  *     call returns, so the calls are not meant for CUDA graph stream capture:
  *     a replayed copy would read released memory.
  *   - Every call returns an attn status code. Argument errors are detected on
- *     the host before anything is enqueued. Device-side errors (a bounded wait
- *     that gave up, an index check that failed) are recorded in the workspace
- *     and read with attn_status(). No entry point traps or aborts.
+ *     the host before anything is enqueued. Device-side errors are recorded in
+ *     the workspace and read with attn_status(): ATTN_E_TIMEOUT (a bounded
+ *     wait gave up) and ATTN_E_BOUNDS (a work descriptor in the workspace did
+ *     not fit the shape or the workspace; every kernel checks each descriptor
+ *     before it forms an address from it, and skips it). No entry point traps
+ *     or aborts.
  */
 #ifndef ATTN_H_
 #define ATTN_H_
@@ -191,17 +194,19 @@ int attn_fwd(const void* q, const void* k, const void* v,
              void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Stage 1 of the forward: the tile kernel. Rows of unsplit chunks (and rows
- * of split chunks whose tile lies wholly before the split) get their final o
- * and lse; the two key-range partials of the remaining rows go to the
- * workspace as fp32. */
+ * of split chunks whose tile lies wholly before the first split point) get
+ * their final o and lse; the key-range partials of the remaining rows (two
+ * for a split at one point, P for kv_split = -P) go to the workspace as
+ * fp32. */
 int attn_fwd_tiles(const void* q, const void* k, const void* v,
                    const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                    void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Stage 2 of the forward: log-sum-exp merge of the partials of re-split
  * chunks (RSA accumulation over key/value blocks, made exact with LSE):
- * LSE = ln(e^{LSE_A} + e^{LSE_B}); O = e^{LSE_A-LSE} O_A + e^{LSE_B-LSE} O_B;
- * a partial with LSE = -inf has weight 0. A no-op when no chunk is split. */
+ * LSE = ln sum_p e^{LSE_p}; O = sum_p e^{LSE_p-LSE} O_p over the parts whose
+ * key range starts at or before the row; a partial with LSE = -inf has
+ * weight 0. A no-op when no chunk is split. */
 int attn_fwd_merge(const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                    void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
@@ -288,17 +293,27 @@ int attn_bwd_chunk(const void* q, const void* k, const void* v, const void* o, c
  * Returns ATTN_E_WORKSPACE when this shape and chunk table need more forward
  * workspace than ATTN_NOALLOC_SCRATCH_BYTES (attn_workspace_size, pass 0);
  * re-split chunks need fp32 partials, so they reach the limit first.
- * The first call on a device looks up the scratch address for that device
- * (with that device current); make that first call before any stream
- * capture. It allocates nothing. All calls share the one scratch area and
- * it keeps the last call's contents (every call rewrites what it reads):
- * calls that overlap on the GPU race with each other, so issue them on one
- * stream, or otherwise one after the other. The device status word of this
- * path (ATTN_E_TIMEOUT / ATTN_E_BOUNDS) lives in that library scratch, which
- * attn_status() cannot be pointed at, so it is not readable by the caller. */
+ * Every call looks up the scratch address in the context current on the
+ * calling thread (nothing is cached, so a device reset or another context on
+ * the device gets its own address); the first call in a context loads the
+ * library's kernels there, so make it before any stream capture. It
+ * allocates nothing. All calls share the one scratch area and it keeps the
+ * last call's contents (every call rewrites what it reads): calls that
+ * overlap on the GPU race with each other, so issue them on one stream, or
+ * otherwise one after the other. Device-side errors of this path are read
+ * with attn_noalloc_status(). */
 int attn_fwd_noalloc(const void* q, const void* k, const void* v,
                      const attn_chunk* chunks, int32_t n, const attn_shape* shape,
                      void* o, float* lse, void* stream);
+
+/* Device error word of attn_fwd_noalloc (its status header lives in the
+ * library's scratch area): synchronises `stream`, then reads and clears it,
+ * like attn_status() does for a caller workspace. Returns ATTN_OK,
+ * ATTN_E_TIMEOUT or ATTN_E_BOUNDS (ATTN_E_CUDA if the read fails). The word
+ * is cleared by every attn_fwd_noalloc call when it starts, and is shared by
+ * all of them, like the rest of the scratch area. No counterpart on the
+ * pages. */
+int attn_noalloc_status(void* stream);
 
 /* ---- status ------------------------------------------------------------ */
 
