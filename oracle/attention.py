@@ -352,12 +352,6 @@ def chunk_backward(q, k, v, do, qb: int, qe: int, cb: int, scale: float, row_blo
     return dq, dk, dv
 
 
-def causal_flops(pairs: int, D: int) -> Tuple[int, int]:
-    """Algorithmic FLOPs of (forward, backward) for ``pairs`` visible (t, j)
-    pairs: 2 GEMMs forward (QK^T, PV) and 5 backward (S, dP, dV, dK, dQ)."""
-    return 4 * D * pairs, 10 * D * pairs
-
-
 # --------------------------------------------------------------------------
 # Closed form for periodic keys: a full-size check of every row and key.
 # --------------------------------------------------------------------------
@@ -403,3 +397,63 @@ def periodic_keys(q, kc, v, do, scale: float):
         R = np.cumsum((W[:, c:c + 1] * do)[::-1], axis=0)[::-1]
         dV[cls == c] = R[cls == c]
     return O, LSE, dQ, dV
+
+
+# --------------------------------------------------------------------------
+# Closed form for periodic queries: a full-size check of every key's dK.
+# --------------------------------------------------------------------------
+
+def _suffix_sums(x):
+    """Inclusive suffix sums along axis 0: out[j] = sum_{t >= j} x[t]."""
+    return np.cumsum(x[::-1], axis=0)[::-1]
+
+
+def periodic_queries(qc, k, v, do, scale: float):
+    """O, LSE, dK and dV of one causal sequence whose queries repeat with
+    period p: q_t = qc[t mod p]; keys, values and dO are arbitrary. The score
+    of row t against key j then depends on t only through its class
+    c = t mod p: s_cj = scale qc[c] . k_j. With E_cj = e^{s_cj - M_c}, where
+    M_c = max_j s_cj (a shift that cancels in P):
+
+        Z_t   = sum_{j <= t} E_cj,       LSE_t = M_c + ln Z_t,       P_tj = E_cj / Z_t
+        O_t   = sum_{j <= t} E_cj v_j / Z_t,                         D_t  = dO_t . O_t
+        R_c(j) = sum_{t >= j, t = c mod p} dO_t / Z_t,   r_c(j) = sum_{t >= j, t = c mod p} D_t / Z_t
+        dV_j  = sum_t P_tj dO_t                      = sum_c E_cj R_c(j)
+        dK_j  = scale sum_t P_tj (dO_t . v_j - D_t) q_t = scale sum_c E_cj (v_j . R_c(j) - r_c(j)) qc[c]
+
+    i.e. the definition's sums regrouped by query class, evaluated with
+    prefix sums over keys (forward) and suffix sums over queries (backward)
+    in O(T p D), so that every key's dK and dV can be checked at full size,
+    including the first keys, whose sums run over the whole sequence. dQ is
+    not produced (its sum needs D x D running sums); the periodic-keys form
+    covers it."""
+    qc, k, v, do = _f64(qc), _f64(k), _f64(v), _f64(do)
+    T, D = k.shape
+    p = qc.shape[0]
+    t = np.arange(T)
+    cls = t % p
+    s = scale * (k @ qc.T)                          # [T keys, p classes]
+    M = s.max(axis=0)
+    E = np.exp(s - M[None, :])
+    O = np.zeros((T, D))
+    LSE = np.zeros(T)
+    Z = np.zeros(T)
+    for c in range(p):
+        rows = cls == c
+        Zc = np.cumsum(E[:, c])                     # Z_t for a row t of class c
+        num = np.cumsum(E[:, c:c + 1] * v, axis=0)  # sum_{j <= t} E_cj v_j
+        Z[rows] = Zc[rows]
+        O[rows] = num[rows] / Zc[rows, None]
+        LSE[rows] = M[c] + np.log(Zc[rows])
+        del num
+    Dt = np.sum(do * O, axis=1)
+    dK = np.zeros((T, D))
+    dV = np.zeros((T, D))
+    for c in range(p):
+        w = np.where(cls == c, 1.0 / Z, 0.0)        # 1/Z_t on the rows of class c
+        R = _suffix_sums(w[:, None] * do)           # R_c(j)
+        r = _suffix_sums(w * Dt)                    # r_c(j)
+        dV += E[:, c:c + 1] * R
+        dK += (scale * E[:, c] * (np.sum(v * R, axis=1) - r))[:, None] * qc[c][None, :]
+        del R
+    return O, LSE, dK, dV

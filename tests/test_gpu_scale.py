@@ -13,7 +13,7 @@ from chunked_causal_attention_gb300.workloads import WORKLOADS, workload_inputs
 from oracle import attention as A
 from oracle import plan as P
 
-from parity import (check_fwd, check_grad, head, invariants_check, lse_head, plan_of, run_gpu,
+from parity import (GRAD_REL_L2, check_fwd, check_grad, head, invariants_check, lse_head, plan_of, run_gpu,
                     sampled_rows_check, tail_keys_check)
 
 pytestmark = pytest.mark.gpu
@@ -142,3 +142,36 @@ def test_7b_128k_multiplex_plan():
     qh, kh, vh = (head(x, 0, 9, False) for x in (q, k, v))
     ro, rl = A.forward_rows(qh, kh, vh, r, w.scale)
     check_fwd(head(o, 0, 9, False)[r], lse_head(lse, 0, 9)[r], ro, rl, "128k multiplex boundaries")
+
+
+@pytest.mark.parametrize("name", ["7b_128k", pytest.param("13b_1m", marks=pytest.mark.slow)])
+def test_periodic_queries_every_key_and_row(name):
+    """Queries repeating with period 3 (q_t = qc[t mod 3]) with random keys,
+    values and dO make the float64 oracle linear in T
+    (oracle.attention.periodic_queries), so dK and dV are checked on every key
+    and O and LSE on every row, of two heads at full size: in the benchmark's
+    launch configuration and plan. The first keys' dK sums over every later
+    query of the sequence (the longest accumulation the backward does)."""
+    from chunked_causal_attention_gb300.workloads import randn_bf16
+    w = WORKLOADS[name]
+    _, k, v, do = workload_inputs(w, device="cuda")
+    p = 3
+    qc = randn_bf16((w.B, w.H, p, w.D), w.seed * 4 + 9, device="cuda")
+    q = qc[:, :, torch.arange(w.L, device="cuda") % p, :].contiguous()
+    chunks = plan_of(w)
+    o, lse, dq, dk, dv = run_gpu(q, k, v, do, chunks)
+    for h in (0, w.H - 1):
+        qch = qc[0, h].float().cpu().numpy().astype(np.float64)
+        ro, rl, rdk, rdv = A.periodic_queries(qch, head(k, 0, h, False), head(v, 0, h, False),
+                                              head(do, 0, h, False), w.scale)
+        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"{name} periodic-q h{h} all rows")
+        gdk, gdv = head(dk, 0, h, False), head(dv, 0, h, False)
+        check_grad(gdk, rdk, f"{name} periodic-q dK h{h} all keys")
+        check_grad(gdv, rdv, f"{name} periodic-q dV h{h} all keys")
+        check_grad(gdk[:4096], rdk[:4096], f"{name} periodic-q dK h{h} first 4096 keys")
+        check_grad(gdk[-4096:], rdk[-4096:], f"{name} periodic-q dK h{h} last 4096 keys")
+        # every 128-key tile on its own: no tile's dK may hide behind the whole-head norm
+        worst = max(float(np.linalg.norm(gdk[t:t + 128] - rdk[t:t + 128]) / np.linalg.norm(rdk[t:t + 128]))
+                    for t in range(0, w.L, 128))
+        assert worst <= GRAD_REL_L2, f"{name} periodic-q dK h{h} worst 128-key tile rel-L2 {worst}"
+        print(f"[parity] {name} periodic-q dK h{h}: worst 128-key tile rel-L2 {worst:.3e}")

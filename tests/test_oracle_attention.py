@@ -230,11 +230,9 @@ def test_sampled_forms_match_full():
     np.testing.assert_allclose(dvk, dv[keys], atol=1e-12)
 
 
-def test_flop_count():
+def test_pair_count():
     pairs = P.causal_pairs(0, 131072, 0)
     assert pairs == 131072 * 131073 // 2 == 8590000128
-    f, b = A.causal_flops(pairs * 32, 128)
-    assert f + b == 14 * 128 * 32 * pairs
 
 
 @pytest.mark.parametrize("T,p,D", [(700, 3, 16), (257, 1, 8), (130, 7, 32)])
@@ -247,6 +245,35 @@ def test_periodic_keys_closed_form_matches_definition(T, p, D):
     Op, Lp, dqp, dvp = A.periodic_keys(q, kc, v, do, sc)
     for a, b in ((Op, O), (Lp, L), (dqp, dq), (dvp, dv)):
         np.testing.assert_allclose(a, b, atol=1e-10, rtol=1e-10)
+
+
+@pytest.mark.parametrize("T,p,D", [(700, 3, 16), (257, 1, 8), (130, 7, 32), (5, 9, 4)])
+def test_periodic_queries_closed_form_matches_definition(T, p, D):
+    """The periodic-queries closed form against the plain definition
+    (A.backward, itself pinned to brute force, torch and finite differences),
+    including a period longer than the sequence."""
+    k, v, do = rand((T, D), 85), rand((T, D), 86), rand((T, D), 87)
+    qc = rand((p, D), 88)
+    q = qc[np.arange(T) % p]
+    sc = 1 / math.sqrt(D)
+    dq, dk, dv, O, L = A.backward(q, k, v, do, sc, None, row_block=64)
+    Op, Lp, dkp, dvp = A.periodic_queries(qc, k, v, do, sc)
+    for a, b in ((Op, O), (Lp, L), (dkp, dk), (dvp, dv)):
+        np.testing.assert_allclose(a, b, atol=1e-10, rtol=1e-10)
+
+
+def test_periodic_queries_against_autograd():
+    """Library pin: torch float64 SDPA and autograd on the periodic queries,
+    with large scores (scale 1) so that the shift by each class's maximum
+    matters."""
+    T, p, D = 300, 4, 16
+    k, v, do = rand((T, D), 95), rand((T, D), 96), rand((T, D), 97)
+    qc = 2.0 * rand((p, D), 98)
+    q = qc[np.arange(T) % p]
+    o, lse, _, tdk, tdv = torch_ref(q, k, v, do, 1.0, [0, T])
+    Op, Lp, dkp, dvp = A.periodic_queries(qc, k, v, do, 1.0)
+    for a, b in ((Op, o), (Lp, lse), (dkp, tdk), (dvp, tdv)):
+        np.testing.assert_allclose(a, b, atol=1e-9, rtol=1e-9)
 
 
 # ---------------------------------------------------- chunk-streamed backward

@@ -395,3 +395,24 @@ def test_infinipipe_threshold_mistake_is_caught(monkeypatch):
         assert plan_threshold(lengths, 2, 2048, cost, max) == IP.plan(lengths, 2, 2048, cost)
     monkeypatch.setattr(IP, "plan", lambda lengths, K, cap, cost: plan_threshold(lengths, K, cap, cost, min))
     assert fails(TI.test_threshold_starts_at_the_costliest_mesh_slice)
+
+
+# ------------------------------------------------------------------ closed forms at full size
+
+def test_periodic_queries_suffix_mistake_is_caught(monkeypatch):
+    def suffix_exclusive(x):
+        # sums over t > j: the diagonal query of every key dropped
+        out = np.cumsum(x[::-1], axis=0)[::-1]
+        return out - x
+    monkeypatch.setattr(A, "_suffix_sums", suffix_exclusive)
+    assert fails(TA.test_periodic_queries_closed_form_matches_definition, 130, 7, 32)
+
+
+def test_periodic_queries_class_mistake_is_caught(monkeypatch):
+    real = A.periodic_queries
+
+    def classes_shifted(qc, k, v, do, scale):
+        # row t read as class (t + 1) mod p: the query period misaligned
+        return real(np.roll(np.asarray(qc), -1, axis=0), k, v, do, scale)
+    monkeypatch.setattr(A, "periodic_queries", classes_shifted)
+    assert fails(TA.test_periodic_queries_closed_form_matches_definition, 700, 3, 16)
