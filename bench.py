@@ -238,7 +238,10 @@ def run_reference(args):
 def workload_config(w, args):
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "tokens": w.L, "plan_chunks": w.N,
            "plan_mode": ["uniform", "flops", "flops_resplit_edges"][w.mode], "packed": w.packed,
-           "l2": "inputs larger than L2 (1 GiB per tensor); no flush", "parallelism": f"replicas x{args.gpus}"}
+           "l2": f"inputs of {w.B * w.H * w.L * w.D * 2 / 2**30:.3g} GiB per tensor, q/k/v/dO together larger "
+                 "than the 129 MB L2; no flush", "parallelism": f"replicas x{args.gpus}"}
+    if getattr(args, "heads", 0):
+        cfg["heads_override"] = args.heads
     if w.Hkv is not None:
         cfg["Hkv"] = w.Hkv
     if args.plan != "default" and not w.packed:
@@ -283,6 +286,12 @@ def run_ours(args):
             dist.barrier()
 
     w = WORKLOADS[args.workload]
+    if args.heads:
+        # fewer heads of the same sequence: a small case for profiler captures (the
+        # backward walks heads one after another, so its traffic per head carries over)
+        import dataclasses
+        g = w.H // (w.Hkv or w.H)
+        w = dataclasses.replace(w, H=args.heads, Hkv=None if w.Hkv is None else max(1, args.heads // g))
     if w.packed:
         chunks = cca.attn_plan_varlen(w.cu_seqlens(), w.max_chunk_tokens, w.mode)
     elif args.plan.startswith("multiplex:"):
@@ -408,7 +417,9 @@ def run_ours(args):
         # host memory and reads its results back. Uploads and read-backs run on two
         # copy streams of their own with two sets of device buffers, so step i+1's
         # upload and step i-1's read-back overlap step i's kernels and each other;
-        # each step still moves all of its own bytes.
+        # each step still moves all of its own bytes. Within a step the forward waits
+        # only for q, k, v (dO's upload overlaps it), and o, lse are read back while
+        # the backward runs.
         e2e_steps = max(8, min(2 * args.steps, 12))   # enough steps that the pipeline's fill and drain stay small
         hin = [x.cpu().pin_memory() for x in (q, k, v, do)]
         hout = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
@@ -420,9 +431,13 @@ def run_ours(args):
         h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         tev = lambda: torch.cuda.Event(enable_timing=True)
         h2d_start = [tev() for _ in range(e2e_steps)]
+        qkv_done = [tev() for _ in range(e2e_steps)]
         h2d_done = [tev() for _ in range(e2e_steps)]
+        fwd_done = [tev() for _ in range(e2e_steps)]
         comp_done = [tev() for _ in range(e2e_steps)]
         d2h_start = [tev() for _ in range(e2e_steps)]
+        d2h_fwd_done = [tev() for _ in range(e2e_steps)]
+        d2h_bwd_start = [tev() for _ in range(e2e_steps)]
         d2h_done = [tev() for _ in range(e2e_steps)]
 
         def e2e_upload(i):
@@ -431,8 +446,10 @@ def run_ours(args):
                 if i >= 2:
                     h2d_stream.wait_event(comp_done[i - 2])       # step i-2 no longer reads these inputs
                 h2d_start[i].record(h2d_stream)
-                for d_, h_ in zip(din, hin):
+                for d_, h_ in zip(din[:3], hin[:3]):
                     d_.copy_(h_, non_blocking=True)
+                qkv_done[i].record(h2d_stream)
+                din[3].copy_(hin[3], non_blocking=True)
                 h2d_done[i].record(h2d_stream)
 
         barrier()
@@ -447,18 +464,25 @@ def run_ours(args):
             din, dout_ = bufs[i % 2]
             q2, k2, v2, do2 = din
             o2, lse2, dq2, dk2, dv2 = dout_
-            stream.wait_event(h2d_done[i])
+            stream.wait_event(qkv_done[i])
             if i >= 2:
                 stream.wait_event(d2h_done[i - 2])               # step i-2's results are read back
             cca.attn_fwd(q2, k2, v2, chunks, shape, o2, lse2, ws_f, stream)
+            fwd_done[i].record(stream)
+            stream.wait_event(h2d_done[i])                       # dO is in
             cca.attn_bwd(q2, k2, v2, o2, lse2, do2, chunks, shape, dq2, dk2, dv2, ws_b, stream)
             comp_done[i].record(stream)
             if i + 1 < e2e_steps:
                 e2e_upload(i + 1)
             with torch.cuda.stream(d2h_stream):
-                d2h_stream.wait_event(comp_done[i])
+                d2h_stream.wait_event(fwd_done[i])               # o, lse while the backward runs
                 d2h_start[i].record(d2h_stream)
-                for h_, d_ in zip(hout, dout_):
+                for h_, d_ in zip(hout[:2], dout_[:2]):
+                    h_.copy_(d_, non_blocking=True)
+                d2h_fwd_done[i].record(d2h_stream)
+                d2h_stream.wait_event(comp_done[i])
+                d2h_bwd_start[i].record(d2h_stream)
+                for h_, d_ in zip(hout[2:], dout_[2:]):
                     h_.copy_(d_, non_blocking=True)
                 d2h_done[i].record(d2h_stream)
         stream.wait_event(d2h_done[e2e_steps - 1])
@@ -466,8 +490,11 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = e0.elapsed_time(e1)
+        # the copies' own time: the dO upload and the dq/dk/dv read-back may wait for
+        # compute, so each group of copies is timed from its own start
         h2d_ms = sum(h2d_start[i].elapsed_time(h2d_done[i]) for i in range(e2e_steps))
-        d2h_ms = sum(d2h_start[i].elapsed_time(d2h_done[i]) for i in range(e2e_steps))
+        d2h_ms = sum(d2h_start[i].elapsed_time(d2h_fwd_done[i]) + d2h_bwd_start[i].elapsed_time(d2h_done[i])
+                     for i in range(e2e_steps))
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
         nbytes = lambda x: x.numel() * x.element_size()
         h2d = sum(nbytes(x) for x in (q, k, v, do))
@@ -475,7 +502,8 @@ def run_ours(args):
         e2e_value = job_tflops(flops_step, e2e_steps, world, e2e_ms)
         return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "copies": "pinned host buffers; upload and read-back streams overlapped with compute",
+                "copies": "pinned host buffers; upload and read-back streams overlapped with compute; the forward "
+                          "waits for q, k, v only, and o, lse are read back during the backward",
                 "h2d_gbs": h2d * e2e_steps / (h2d_ms * 1e-3) / 1e9,
                 "d2h_gbs": d2h * e2e_steps / (d2h_ms * 1e-3) / 1e9}
 
@@ -508,7 +536,7 @@ def run_ours(args):
             "roofline": {"kernel": "bwd key-tile kernel (attn_bwd_tiles)", "bound": "tensor",
                          "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
                          "peak_kind": f"bf16_tflops_sustained ({peak_src})",
-                         "frac_of_burst": achieved / peak_burst, "traffic": measured_traffic(w.name),
+                         "frac_of_burst": achieved / peak_burst, "traffic": None if args.heads else measured_traffic(w.name),
                          "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
             "hbm_kernels": hbm_kernels(w, chunks, stage_ms, peaks["hbm_gbs"]),
             "gpu_launches": launches_per_step * args.steps,
@@ -543,6 +571,8 @@ def main():
                     help="report the device-timed leg only (no chunk-streamed and no end-to-end leg)")
     ap.add_argument("--plan", default="default",
                     help="default (the workload's plan) or multiplex:PP (SPPO Table 3 edge re-splits)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads instead of its own (small profiler captures)")
     ap.add_argument("--clock-log", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed region to this CSV file")
     args = ap.parse_args()

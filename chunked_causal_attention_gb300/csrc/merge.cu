@@ -65,11 +65,16 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
     const int64_t blk = sg.blk;
     const int32_t* kb = a.kbounds + sg.kb;
     // parts whose key range starts at or before this row (at least part 0,
-    // which starts at the document start)
-    int np = 0;
-    for (int p0 = 0; p0 < sg.P; p0 += 32) {
-        const int p = p0 + lane;
-        np += __popc(__ballot_sync(0xffffffffu, p < sg.P && kb[p] <= t));
+    // which starts at the document start). A split at one point needs no count:
+    // the forward writes both partials of every row of the segment (part 1 with
+    // LSE = -inf where the row sees none of its keys, which gives it weight 0).
+    int np = 2;
+    if (sg.P != 2) {
+        np = 0;
+        for (int p0 = 0; p0 < sg.P; p0 += 32) {
+            const int p = p0 + lane;
+            np += __popc(__ballot_sync(0xffffffffu, p < sg.P && kb[p] <= t));
+        }
     }
     // part p's LSE is at lse_row[p * blk], its O row at o_row[p * blk]
     const float* lse_row = a.ws_f + sg.off0 + (int64_t)BH * R * D + (int64_t)bh * R + i;

@@ -69,6 +69,9 @@ def test_workload_config(name):
     assert "model" not in cfg
     if w.Hkv is not None:
         assert cfg["Hkv"] == w.Hkv
+    assert "heads_override" not in cfg
+    small = bench.workload_config(w, types.SimpleNamespace(gpus=1, plan="default", heads=2))
+    assert small["heads_override"] == 2
 
 
 def test_reference_arm_under_torchrun_prints_from_rank_0_only():
