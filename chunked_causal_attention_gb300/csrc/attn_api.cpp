@@ -291,6 +291,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
             a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.ws_f = ws_f;
             a.part_floats = L.part_floats;
             a.status = (uint32_t*)ws;
+            a.counter = &((WsHeader*)ws)->counter[0];   // zeroed with the header above
             a.items = (const FwdItem*)(w + L.off_items);
             a.n_items = (int32_t)L.items.size();
             a.group = kGroupFwd;
@@ -347,8 +348,13 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
         } else if ((st = upload(w + L.off_items, L.items.data(), L.items.size() * sizeof(BwdItem), s))) {
             return st;
         }
+        // the tile kernel's work queue starts at zero (the status word is kept: an
+        // earlier stage of the same backward may have recorded an error)
+        uint32_t* counter = &((WsHeader*)ws)->counter[1];
+        if (cudaMemsetAsync(counter, 0, sizeof(uint32_t), s) != cudaSuccess) return ATTN_E_CUDA;
         BwdArgs a;
         a.q = q; a.k = k; a.v = v; a.dout = dout; a.lse = lse; a.delta = delta;
+        a.counter = counter;
         a.dk = dk; a.dv = dv; a.dq_acc = dq_acc;
         a.rows = L.rows;
         a.dk_acc = dk_acc; a.dv_acc = dv_acc;

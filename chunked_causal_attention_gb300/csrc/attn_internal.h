@@ -18,7 +18,7 @@ constexpr size_t kHeaderBytes = 256;  // workspace header: status word, counters
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
     uint32_t status;      // first device-side error code (ATTN_E_*), 0 if none
-    uint32_t counter[3];  // work counters of persistent kernels
+    uint32_t counter[3];  // work queues of the persistent kernels: [0] forward tiles, [1] backward tiles
 };
 
 // One forward work item: query rows [r0, r1) against keys [kv_lo, kv_hi)
@@ -92,6 +92,7 @@ struct FwdArgs {
     float* ws_f;
     int64_t part_floats;  // floats of the partial region at ws_f (index checks)
     uint32_t* status;
+    uint32_t* counter;    // work queue: next work index to hand out (zero at launch)
     const FwdItem* items;
     int32_t n_items;
     int32_t group;        // items per head group in the work order
@@ -135,6 +136,7 @@ struct BwdArgs {
     // keys >= the item's emit_from. Null for the whole backward (bf16 written).
     float* dk_acc; float* dv_acc;
     uint32_t* status;
+    uint32_t* counter;    // work queue: next work index to hand out (zero at launch)
     const BwdItem* items;
     int32_t n_items;
     int32_t group;

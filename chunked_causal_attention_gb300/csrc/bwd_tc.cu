@@ -76,7 +76,8 @@ struct BwdTcLayout {
     static constexpr int B_SDP = 6, B_PCH = 7;         // B_PCH + c: P^T/dS^T of query chunk c ready
     static constexpr int B_DQFULL = 11, B_DQFREE = 12;
     static constexpr int B_DKDVFULL = 13, B_DKDVFREE = 14, B_DRAIN = 15;
-    static constexpr int NBAR = 16;
+    static constexpr int B_RFULL = 16, B_REMPTY = 18;  // work ring: 2 slots each
+    static constexpr int NBAR = 20;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr size_t ALLOC = (size_t)BYTES + 1024;
@@ -189,6 +190,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                   const __grid_constant__ CUtensorMap tmdq, const __grid_constant__ AccMaps<ACC> am,
                   const BwdArgs a, const TcMaps mp, const TcMaps mpkv, const int32_t n_work) {
     using LY = BwdTcLayout<D>;
+    // every item comes from the work queue (see WorkRing); its consumers are the
+    // MMA thread, the 8 softmax-gradient warps and the 4 drain warps
     constexpr uint32_t kColDK = kColDV + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -199,6 +202,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC_OFF + 4);
     float* s_nl = reinterpret_cast<float*>(sm + LY::NL_OFF);
     float* s_nd = reinterpret_cast<float*>(sm + LY::ND_OFF);
+    const WorkRing ring{reinterpret_cast<volatile int32_t*>(sm + LY::MISC_OFF + 8), bar(LY::B_RFULL),
+                        bar(LY::B_REMPTY)};
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int BHKV = a.g.B * a.g.Hkv;            // work items run over (key tile, batch, key/value head)
@@ -218,6 +223,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         mbar_init(bar(LY::B_DKDVFULL), 1);
         mbar_init(bar(LY::B_DKDVFREE), 256);
         mbar_init(bar(LY::B_DRAIN), 1);
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(bar(LY::B_RFULL + r), 1);
+            mbar_init(bar(LY::B_REMPTY + r), 13);      // MMA thread, 8 + 4 consumer warps
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -239,7 +248,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tma_prefetch_desc(&tmdo);
             uint32_t qc = 0, ic = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < n_work && !a.stall && ok && !*abort_flag; w += gridDim.x, ++ic) {
+            int32_t w = a.stall ? n_work : (int32_t)atomicAdd(a.counter, 1u);
+            for (; !a.stall && ok; ++ic) {
+                // publish the item (or the end of the work) to the consumers
+                ok = ring_put(ring, ic, w < n_work ? w : -1, abort_flag, a.status, a.wait_ns);
+                if (!ok || w >= n_work || *abort_flag) break;
                 int32_t it, bkv;
                 decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
@@ -248,6 +261,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     *abort_flag = 1;
                     break;
                 }
+                int32_t w_next = n_work;
                 const int b = bkv / a.g.Hkv, hk = bkv % a.g.Hkv;
                 ok = mbar_wait(bar(LY::B_KVEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
@@ -265,7 +279,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                     const uint32_t st = sbase + LY::QDO_OFF + s * LY::STAGE;
                     load_tile_b<D>(st, &tmq, bar(LY::B_QFULL + s), mp, row, hk * G + g, b);
                     load_tile_b<D>(st + LY::TILE, &tmdo, bar(LY::B_QFULL + s), mp, row, hk * G + g, b);
+                    // the item's last loads are out: claim the next item now, about two
+                    // blocks before this CTA is free for it
+                    if (blk == G * nq - 1) w_next = (int32_t)atomicAdd(a.counter, 1u);
                 }
+                w = w_next;
             }
         }
     } else if (warp == 1) {
@@ -277,7 +295,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const uint32_t k0 = sbase + LY::K_OFF, v0 = sbase + LY::V_OFF, ds0 = sbase + LY::DS_OFF;
             uint32_t qc = 0, ic = 0, gb = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+            for (; ok; ++ic) {
+                int32_t w = -1;
+                ok = ring_get(ring, ic, w, abort_flag, a.status, a.wait_ns);
+                if (!ok || w < 0 || *abort_flag) break;
                 int32_t it, bkv;
                 decode_work(w, a.n_items, BHKV, a.group, it, bkv);
                 const BwdItem item = a.items[it];
@@ -366,7 +387,15 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         // the loop on its own: `ok` changes only through a group vote
         // (named_sync_all), which every thread of the group reaches, and the item
         // check gives the same answer in every thread.
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++ic) {
+        for (; ok; ++ic) {
+            // the next item: every warp reads it, and the group goes on only if all did
+            int32_t w = -1;
+            const bool got = ring_get_warp(ring, ic, w, abort_flag, a.status, a.wait_ns);
+            if (!named_sync_all(1 + grp, 128, got && !*abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;                            // no more work (the same w in every thread)
             int32_t it, bkv;
             decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];
@@ -544,7 +573,15 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         bool ok = true;
         // as in the softmax-gradient groups, the four warps leave only together,
         // by the vote at their barrier (`ok` is the same in every thread)
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+        for (uint32_t ic = 0; ok; ++ic) {
+            // the next item: every warp reads it, and the group goes on only if all did
+            int32_t w = -1;
+            const bool got = ring_get_warp(ring, ic, w, abort_flag, a.status, a.wait_ns);
+            if (!named_sync_all(3, 128, got && !*abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;                            // no more work (the same w in every thread)
             int32_t it, bkv;
             decode_work(w, a.n_items, BHKV, a.group, it, bkv);
             const BwdItem item = a.items[it];

@@ -65,8 +65,9 @@ struct FwdTcLayout {
     static constexpr int B_OFREE = B_ODONE + 1;
     static constexpr int B_OFULL = B_OFREE + 1;                // last PV of an item complete
     static constexpr int B_DRAIN = B_OFULL + 1;
-    static constexpr int NBAR = B_DRAIN + 1;
-    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;        // tmem base (u32), abort flag (int)
+    static constexpr int B_RFULL = B_DRAIN + 1, B_REMPTY = B_RFULL + 2;   // work ring: 2 slots each
+    static constexpr int NBAR = B_REMPTY + 2;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;        // tmem base (u32), abort flag (int), work ring (2 x i32)
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr size_t ALLOC = (size_t)BYTES + 1024;      // slack for 1024-byte alignment
 };
@@ -95,6 +96,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC_OFF + 4);
+    // every item comes from the work queue (see WorkRing); its consumers are the
+    // MMA thread and the 4 softmax warps
+    const WorkRing ring{reinterpret_cast<volatile int32_t*>(sm + LY::MISC_OFF + 8), bar(LY::B_RFULL),
+                        bar(LY::B_REMPTY)};
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int BH = a.g.B * a.g.H;
@@ -116,6 +121,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init(bar(LY::B_OFREE), 128);
         mbar_init(bar(LY::B_OFULL), 1);
         mbar_init(bar(LY::B_DRAIN), 1);
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(bar(LY::B_RFULL + r), 1);
+            mbar_init(bar(LY::B_REMPTY + r), 5);       // MMA thread, 4 softmax warps
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -135,7 +144,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
             uint32_t kc = 0, vc = 0, ic = 0;
-            for (int w = blockIdx.x; w < n_work && !a.stall && !*abort_flag; w += gridDim.x, ++ic) {
+            int32_t w = a.stall ? n_work : (int32_t)atomicAdd(a.counter, 1u);
+            for (; !a.stall; ++ic) {
+                // publish the item (or the end of the work) to the consumers
+                if (!ring_put(ring, ic, w < n_work ? w : -1, abort_flag, a.status, a.wait_ns)) break;
+                if (w >= n_work || *abort_flag) break;
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 load_tile<D>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
                 const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
                 bool ok = true;
+                int32_t w_next = n_work;
                 for (int j = 0; j < nblk && ok; ++j) {
                     const int row = item.kv_lo + j * 128;
                     const uint32_t ks = kc % KV_STAGES, vs = vc % KV_STAGES;
@@ -164,8 +178,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE);
                     load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mpkv, row, hk, b);
                     ++vc;
+                    // the item's last loads are out: claim the next item now, a block or
+                    // two before this CTA is free for it
+                    if (j == nblk - 1) w_next = (int32_t)atomicAdd(a.counter, 1u);
                 }
                 if (!ok) break;
+                w = w_next;
             }
         }
     } else if (warp == 1) {
@@ -175,7 +193,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);
             uint32_t kc = 0, vc = 0, ic = 0, gt = 0;   // gt: global tile counter (S buffer, P, PV index)
             bool ok = true;
-            for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+            for (; ok; ++ic) {
+                int32_t w = -1;
+                ok = ring_get(ring, ic, w, abort_flag, a.status, a.wait_ns);
+                if (!ok || w < 0 || *abort_flag) break;
                 int32_t it, bh;
                 decode_work(w, a.n_items, BH, a.group, it, bh);
                 const FwdItem item = a.items[it];
@@ -246,7 +267,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const float sl2 = a.g.scale * kLog2e;
         uint32_t gt = 0, ic = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < n_work && ok && !*abort_flag; w += gridDim.x, ++ic) {
+        for (; ok; ++ic) {
+            // each softmax warp reads the next item on its own (they meet no named barrier)
+            int32_t w = -1;
+            ok = ring_get_warp(ring, ic, w, abort_flag, a.status, a.wait_ns);
+            if (!ok || w < 0 || *abort_flag) break;
             int32_t it, bh;
             decode_work(w, a.n_items, BH, a.group, it, bh);
             const FwdItem item = a.items[it];

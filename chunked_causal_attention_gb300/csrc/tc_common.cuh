@@ -76,6 +76,51 @@ __device__ __forceinline__ bool named_sync_all(int id, int n, bool pred) {
     return r != 0;
 }
 
+// ------------------------------------------------------------------ work queue
+// The work of a persistent kernel comes from a counter in global memory. The
+// producer thread claims work indices with atomicAdd, claiming the next one a
+// little before its current item ends, so that items go to CTAs in the order in
+// which the CTAs become free: greedy list scheduling of the heaviest-first work
+// list. It hands each index to the CTA's consumer roles through a two-slot ring
+// in shared memory: slot s holds a work index (or -1: no more work),
+// full[s] (count 1) says it is written, empty[s] (one arrival per consumer) that
+// every consumer has read it.
+struct WorkRing {
+    volatile int32_t* slot;   // 2 entries
+    uint32_t full, empty;     // mbarriers of slot 0; those of slot 1 follow at +8
+};
+
+// Producer: publish work index w as the ic-th item.
+__device__ __forceinline__ bool ring_put(const WorkRing& r, uint32_t ic, int32_t w, volatile int* abort,
+                                         uint32_t* status, uint64_t limit_ns) {
+    const uint32_t s = ic & 1;
+    if (!mbar_wait(r.empty + 8 * s, ((ic >> 1) & 1) ^ 1, abort, status, limit_ns)) return false;
+    r.slot[s] = w;
+    mbar_arrive(r.full + 8 * s);
+    return true;
+}
+
+// A consumer that is one thread (it counts once in empty[s]).
+__device__ __forceinline__ bool ring_get(const WorkRing& r, uint32_t ic, int32_t& w, volatile int* abort,
+                                         uint32_t* status, uint64_t limit_ns) {
+    const uint32_t s = ic & 1;
+    if (!mbar_wait(r.full + 8 * s, (ic >> 1) & 1, abort, status, limit_ns)) return false;
+    w = r.slot[s];
+    mbar_arrive(r.empty + 8 * s);
+    return true;
+}
+
+// A consumer that is a whole warp (it counts once in empty[s]): every lane gets w.
+__device__ __forceinline__ bool ring_get_warp(const WorkRing& r, uint32_t ic, int32_t& w, volatile int* abort,
+                                              uint32_t* status, uint64_t limit_ns) {
+    const uint32_t s = ic & 1;
+    if (!mbar_wait_warp(r.full + 8 * s, (ic >> 1) & 1, abort, status, limit_ns)) return false;
+    w = r.slot[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(r.empty + 8 * s);
+    return true;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
