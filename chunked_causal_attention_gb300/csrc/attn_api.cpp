@@ -18,12 +18,17 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Head dims: the forward takes any multiple of 8 up to 256, the backward up to
+// 128 (its dK and dV accumulators of a 256-wide tile would fill TMEM alone).
+constexpr int64_t kMaxDimFwd = 256;
+constexpr int64_t kMaxDimBwd = 128;
+
 int check_shape(const attn_shape* s, Geom* g) {
     if (!s) return ATTN_E_INVAL;
     if (s->B <= 0 || s->H <= 0 || s->T <= 0 || s->D <= 0) return ATTN_E_INVAL;
     if (s->T > INT32_MAX || s->B > INT32_MAX || s->H > INT32_MAX) return ATTN_E_INVAL;
     if ((int64_t)s->B * s->H > (1ll << 24)) return ATTN_E_INVAL;
-    if (s->D < 8 || s->D > 128 || (s->D % 8)) return ATTN_E_UNSUPPORTED;
+    if (s->D < 8 || s->D > kMaxDimFwd || (s->D % 8)) return ATTN_E_UNSUPPORTED;
     if (s->sb <= 0 || s->st <= 0 || s->sh <= 0) return ATTN_E_INVAL;
     if (!std::isfinite(s->scale)) return ATTN_E_INVAL;
     if ((s->sb % 8) || (s->st % 8) || (s->sh % 8)) return ATTN_E_ALIGN;
@@ -379,6 +384,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
     Geom g;
     int st = check_shape(shape, &g);
     if (st) return st;
+    if (g.D > kMaxDimBwd) return ATTN_E_UNSUPPORTED;
     if ((st = check_chunks_bwd(chunks, n, g.T))) return st;
     if ((stages & kPrep) && (!o || !dout)) return ATTN_E_INVAL;
     if ((stages & kTiles) && (!q || !k || !v || !lse || !dout || !dk || !dv)) return ATTN_E_INVAL;
@@ -408,11 +414,13 @@ int attn_workspace_size(const attn_shape* shape, const attn_chunk* chunks, int32
         fwd_layout(g, chunks, n, L);
         *bytes = L.bytes;
     } else if (pass == 1) {
+        if (g.D > kMaxDimBwd) return ATTN_E_UNSUPPORTED;
         if ((st = check_chunks_bwd(chunks, n, g.T))) return st;
         BwdLayout L;
         bwd_layout(g, chunks, n, L);
         *bytes = L.bytes;
     } else if (pass == 2) {
+        if (g.D > kMaxDimBwd) return ATTN_E_UNSUPPORTED;
         if ((st = check_chunks_stream(chunks, n, g.T))) return st;
         BwdLayout L;
         bwd_chunk_layout(g, chunks, n, L);
@@ -472,6 +480,7 @@ int attn_bwd_chunk(const void* q, const void* k, const void* v, const void* o, c
     Geom g;
     int st = check_shape(shape, &g);
     if (st) return st;
+    if (g.D > kMaxDimBwd) return ATTN_E_UNSUPPORTED;
     if ((st = check_chunks_stream(chunks, n, g.T))) return st;
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, dk_acc, dv_acc};
     for (const void* p : ptrs)

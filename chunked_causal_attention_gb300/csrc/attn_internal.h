@@ -171,8 +171,8 @@ struct TcMaps {
 
 // Rank-4 TMA map of a bf16 [B, T, H, D]-strided tensor: axis 0 is the head
 // dim, axes 1..3 are token/head/batch sorted by stride; box = 64 elements
-// (128 bytes, 128-byte swizzle) x 128 tokens. Fills `mp`. False on failure.
-bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp);
+// (128 bytes, 128-byte swizzle) x box_rows tokens. Fills `mp`. False on failure.
+bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, int box_rows = 128);
 // Rank-3 TMA map of the fp32 dQ accumulator [B*H][rows][D]: box of 32 floats
 // (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
 bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);

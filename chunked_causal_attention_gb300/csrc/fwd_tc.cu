@@ -48,13 +48,21 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
+// Keys per K/V tile: 128, or 64 for the 256-wide head dims, whose Q tile (64 KB)
+// and two-stage K and V rings (4 x 32 KB) then fit in shared memory, and whose
+// two S buffers (2 x 64 columns) and O (256 columns) fit in TMEM.
+template <int D>
+constexpr int kBlockN = D > 128 ? 64 : 128;
+
 template <int D>
 struct FwdTcLayout {
-    static constexpr int TILE = 128 * D * 2;            // bytes of one 128-row bf16 tile
+    static constexpr int BN = kBlockN<D>;
+    static constexpr int TILE_Q = 128 * D * 2;          // bytes of the 128-row bf16 Q tile
+    static constexpr int TILE_KV = BN * D * 2;          // bytes of one BN-row bf16 K or V tile
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + TILE;
-    static constexpr int V_OFF = K_OFF + KV_STAGES * TILE;
-    static constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE;
+    static constexpr int K_OFF = Q_OFF + TILE_Q;
+    static constexpr int V_OFF = K_OFF + KV_STAGES * TILE_KV;
+    static constexpr int BAR_OFF = V_OFF + KV_STAGES * TILE_KV;
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = 1;
     static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + KV_STAGES;
@@ -72,7 +80,9 @@ struct FwdTcLayout {
     static constexpr size_t ALLOC = (size_t)BYTES + 1024;      // slack for 1024-byte alignment
 };
 
-template <int D>
+// One tile of ROWS rows x D dims: D / 64 boxes of 64 dims (128 bytes, 128-byte
+// swizzle) x ROWS rows, box a at dst + a * ROWS * 128.
+template <int D, int ROWS>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, const TcMaps& mp,
                                           int row, int h, int b) {
     // coordinates of map axes 1..3 (token, head, batch in stride order), by selects
@@ -80,7 +90,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
     const int c2 = mp.pos_t == 2 ? row : (mp.pos_h == 2 ? h : b);
     const int c3 = mp.pos_t == 3 ? row : (mp.pos_h == 3 ? h : b);
 #pragma unroll
-    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * 16384, map, bar, a * 64, c1, c2, c3);
+    for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * ROWS * 128, map, bar, a * 64, c1, c2, c3);
 }
 
 template <int D>
@@ -89,6 +99,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                   const __grid_constant__ CUtensorMap tmv, const FwdArgs a, const TcMaps mp, const TcMaps mpkv,
                   const int32_t n_work) {
     using LY = FwdTcLayout<D>;
+    constexpr int BN = LY::BN;                  // keys per K/V tile and columns per S buffer
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -160,23 +171,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int b = bh / a.g.H, h = bh % a.g.H;
                 const int hk = h / (a.g.H / a.g.Hkv);
                 if (!mbar_wait(bar(LY::B_QEMPTY), (ic & 1) ^ 1, abort_flag, a.status, a.wait_ns)) break;
-                mbar_expect_tx(bar(LY::B_QFULL), LY::TILE);
-                load_tile<D>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
-                const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+                mbar_expect_tx(bar(LY::B_QFULL), LY::TILE_Q);
+                load_tile<D, 128>(sbase + LY::Q_OFF, &tmq, bar(LY::B_QFULL), mp, item.r0, h, b);
+                const int nblk = (item.kv_hi - item.kv_lo + BN - 1) / BN;
                 bool ok = true;
                 int32_t w_next = n_work;
                 for (int j = 0; j < nblk && ok; ++j) {
-                    const int row = item.kv_lo + j * 128;
+                    const int row = item.kv_lo + j * BN;
                     const uint32_t ks = kc % KV_STAGES, vs = vc % KV_STAGES;
                     ok = mbar_wait(bar(LY::B_KEMPTY + ks), ((kc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
-                    mbar_expect_tx(bar(LY::B_KFULL + ks), LY::TILE);
-                    load_tile<D>(sbase + LY::K_OFF + ks * LY::TILE, &tmk, bar(LY::B_KFULL + ks), mpkv, row, hk, b);
+                    mbar_expect_tx(bar(LY::B_KFULL + ks), LY::TILE_KV);
+                    load_tile<D, BN>(sbase + LY::K_OFF + ks * LY::TILE_KV, &tmk, bar(LY::B_KFULL + ks), mpkv, row, hk, b);
                     ++kc;
                     ok = mbar_wait(bar(LY::B_VEMPTY + vs), ((vc / KV_STAGES) & 1) ^ 1, abort_flag, a.status, a.wait_ns);
                     if (!ok) break;
-                    mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE);
-                    load_tile<D>(sbase + LY::V_OFF + vs * LY::TILE, &tmv, bar(LY::B_VFULL + vs), mpkv, row, hk, b);
+                    mbar_expect_tx(bar(LY::B_VFULL + vs), LY::TILE_KV);
+                    load_tile<D, BN>(sbase + LY::V_OFF + vs * LY::TILE_KV, &tmv, bar(LY::B_VFULL + vs), mpkv, row, hk, b);
                     ++vc;
                     // the item's last loads are out: claim the next item now, a block or
                     // two before this CTA is free for it
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (elect_one()) {
-            constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_s = idesc_bf16(128, BN, 0, 0);
             constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);
             uint32_t kc = 0, vc = 0, ic = 0, gt = 0;   // gt: global tile counter (S buffer, P, PV index)
             bool ok = true;
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+                const int nblk = (item.kv_hi - item.kv_lo + BN - 1) / BN;
                 ok = mbar_wait(bar(LY::B_QFULL), ic & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
@@ -218,12 +229,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ok = mbar_wait(bar(LY::B_KFULL + ks), (kc / KV_STAGES) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t k0 = sbase + LY::K_OFF + ks * LY::TILE;
-                        const uint32_t sb = tmem + kColS + ((gt + j) & 1) * 128;
+                        const uint32_t k0 = sbase + LY::K_OFF + ks * LY::TILE_KV;
+                        const uint32_t sb = tmem + kColS + ((gt + j) & 1) * BN;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(sb, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s, kk > 0);
+                            // k-step kk: box kk / 4 (64 dims), 32 bytes further per 16 dims
+                            const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+                            mma_ss(sb, sdesc_sw128(q0 + qoff, 16, 1024), sdesc_sw128(k0 + koff, 16, 1024), id_s, kk > 0);
                         }
                         mma_commit(bar(LY::B_KEMPTY + ks));
                         mma_commit(bar(LY::B_SFULL + ((gt + j) & 1)));
@@ -244,11 +257,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ok = mbar_wait(bar(LY::B_VFULL + vs), (pv_vc / KV_STAGES) & 1, abort_flag, a.status, a.wait_ns);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t v0 = sbase + LY::V_OFF + vs * LY::TILE;
-                        const uint32_t pa = tmem + kColS + pb * 128;
+                        const uint32_t v0 = sbase + LY::V_OFF + vs * LY::TILE_KV;
+                        const uint32_t pa = tmem + kColS + pb * BN;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tmem + kColO, pa + kk * 8, sdesc_sw128(v0 + kk * 2048, 16384, 1024), id_o,
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_ts(tmem + kColO, pa + kk * 8, sdesc_sw128(v0 + kk * 2048, BN * 128, 1024), id_o,
                                    (j - 1 > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(bar(LY::B_VEMPTY + vs));
                         mma_commit(bar(LY::B_ODONE));
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 *abort_flag = 1;
                 break;
             }
-            const int nblk = (item.kv_hi - item.kv_lo + 127) / 128;
+            const int nblk = (item.kv_hi - item.kv_lo + BN - 1) / BN;
             const int t_row = item.r0 + row;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nblk && ok; ++j) {
@@ -288,18 +301,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 ok = mbar_wait_warp(bar(LY::B_SFULL + b), (t >> 1) & 1, abort_flag, a.status, a.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sa = tmem + lane_addr + kColS + b * 128;
-                uint32_t r[4][32];
+                constexpr int NC = BN / 32;                // 32-column chunks of an S tile
+                const uint32_t sa = tmem + lane_addr + kColS + b * BN;
+                uint32_t r[NC][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(sa + c * 32, r[c]);
+                for (int c = 0; c < NC; ++c) tmem_ld32(sa + c * 32, r[c]);
                 tmem_ld_wait();
-                const int j0 = item.kv_lo + j * 128;
-                const bool edge = (j0 + 127 > item.r0) || (j0 + 128 > item.kv_hi);
+                const int j0 = item.kv_lo + j * BN;
+                const bool edge = (j0 + BN - 1 > item.r0) || (j0 + BN > item.kv_hi);
                 float mt = -INFINITY;
                 if (edge) {
                     const int lim = min(t_row + 1, item.kv_hi) - j0;   // visible columns: c < lim
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < NC; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             float x = __uint_as_float(r[c][i]);
@@ -311,10 +325,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // four independent chains of three-input maxima
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < NC; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; i += 2)
-                            m4[c] = fmax3(m4[c], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+                            m4[(c * 2 + (i >> 4)) & 3] =
+                                fmax3(m4[(c * 2 + (i >> 4)) & 3], __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
                     mt = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
                 }
                 mt *= sl2;
@@ -331,9 +346,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // exponents two at a time (f32x2 FMA), row sum in two paired accumulators
                 const float2 sl2x2 = make_float2(sl2, sl2), nbase = make_float2(-base, -base);
                 float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                uint32_t p[2][32];
+                uint32_t p[NC / 2][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < NC; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const float2 x =
@@ -344,8 +359,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 const float lsum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
                 l_run = rescale ? fmaf(l_run, alpha, lsum) : l_run + lsum;
-                tmem_st32(sa + 0, p[0]);
-                tmem_st32(sa + 32, p[1]);
+#pragma unroll
+                for (int c2 = 0; c2 < NC / 2; ++c2) tmem_st32(sa + 32 * c2, p[c2]);
                 // tcgen05.ld/st are warp-collective: rescale O if any row of the warp needs it
                 if (__any_sync(0xffffffffu, rescale) && j > 0) {
                     // O holds the sum over tiles < j once PV_{j-1} has completed
@@ -454,8 +469,8 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
     const Geom gkv = a.g.kv();
-    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, gkv, mpkv) ||
-        !make_tile_map(&mv, a.v, gkv, mpkv))
+    if (!make_tile_map(&mq, a.q, a.g, mp) || !make_tile_map(&mk, a.k, gkv, mpkv, kBlockN<D>) ||
+        !make_tile_map(&mv, a.v, gkv, mpkv, kBlockN<D>))
         return cudaErrorInvalidValue;
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
     if (work <= 0) return cudaSuccess;
@@ -471,7 +486,9 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s) {
-    // head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles
+    // head dims up to 64 run on 64-wide tiles, up to 128 on 128-wide tiles, the
+    // others (up to 256) on 256-wide tiles with 64-key K/V tiles
+    if (a.g.D > 128) return launch_d<256>(a, s);
     return a.g.D > 64 ? launch_d<128>(a, s) : launch_d<64>(a, s);
 }
 

@@ -22,6 +22,10 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
+__device__ __forceinline__ float4 fma4(float e, float4 v, float4 r) {
+    return make_float4(fmaf(e, v.x, r.x), fmaf(e, v.y, r.y), fmaf(e, v.z, r.z), fmaf(e, v.w, r.w));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
@@ -29,12 +33,14 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // One warp per (segment row, batch*head): merge the row's partials. Lane l
-// takes the four elements from d = 4l (D is a multiple of 8, at most 128).
+// takes the four elements from d = 4l, and for NH = 2 (head dims above 128)
+// also the four from d = 4l + 128 (D is a multiple of 8, at most 128 * NH).
 // The row's loads go out in few dependent rounds: the parts it sees (a
 // prefix of the segment's increasing key boundaries) are counted by one
 // ballot; then lane p reads part p's LSE while every lane reads its slice of
 // the first two parts' O; the weights reach all lanes by shuffles.
-__global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
+template <int NH>
+__global__ void __launch_bounds__(256, NH == 1 ? 5 : 4) merge_kernel(MergeArgs a) {
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= a.total_work) return;   // the same w for every lane of a warp
@@ -79,14 +85,17 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
     // part p's LSE is at lse_row[p * blk], its O row at o_row[p * blk]
     const float* lse_row = a.ws_f + sg.off0 + (int64_t)BH * R * D + (int64_t)bh * R + i;
     const float* o_row = a.ws_f + sg.off0 + ((int64_t)bh * R + i) * D;
-    const int d = 4 * lane;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 v0 = zero, v1 = zero;
-    if (d < D) {
-        v0 = *reinterpret_cast<const float4*>(o_row + d);
-        if (np > 1) v1 = *reinterpret_cast<const float4*>(o_row + blk + d);
+    float4 v0[NH], v1[NH], r[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        const int d = 4 * lane + 128 * hh;
+        v0[hh] = v1[hh] = r[hh] = zero;
+        if (d < D) {
+            v0[hh] = *reinterpret_cast<const float4*>(o_row + d);
+            if (np > 1) v1[hh] = *reinterpret_cast<const float4*>(o_row + blk + d);
+        }
     }
-    float4 r = zero;
     float tot = 0.f, mx;
     if (np <= 2) {
         // two parts at most (every split of one point): lanes 0 and 1 read the LSEs
@@ -97,12 +106,14 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
             if (l0 != -INFINITY) {
                 const float e = __expf(l0 - mx);
                 tot += e;
-                r = make_float4(fmaf(e, v0.x, r.x), fmaf(e, v0.y, r.y), fmaf(e, v0.z, r.z), fmaf(e, v0.w, r.w));
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) r[hh] = fma4(e, v0[hh], r[hh]);
             }
             if (l1 != -INFINITY) {
                 const float e = __expf(l1 - mx);
                 tot += e;
-                r = make_float4(fmaf(e, v1.x, r.x), fmaf(e, v1.y, r.y), fmaf(e, v1.z, r.z), fmaf(e, v1.w, r.w));
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) r[hh] = fma4(e, v1[hh], r[hh]);
             }
         }
     } else {
@@ -125,10 +136,13 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
             for (int j = 0; j < cnt; ++j) {
                 const float ej = __shfl_sync(0xffffffffu, e, j);
                 const int pj = p0 + j;
-                float4 v = pj == 0 ? v0 : v1;
-                if (pj > 1 && d < D) v = *reinterpret_cast<const float4*>(o_row + pj * blk + d);
-                if (ej != 0.f)
-                    r = make_float4(fmaf(ej, v.x, r.x), fmaf(ej, v.y, r.y), fmaf(ej, v.z, r.z), fmaf(ej, v.w, r.w));
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh) {
+                    const int d = 4 * lane + 128 * hh;
+                    float4 v = pj == 0 ? v0[hh] : v1[hh];
+                    if (pj > 1 && d < D) v = *reinterpret_cast<const float4*>(o_row + pj * blk + d);
+                    if (ej != 0.f) r[hh] = fma4(ej, v, r[hh]);
+                }
             }
         }
     }
@@ -136,15 +150,23 @@ __global__ void __launch_bounds__(256, 5) merge_kernel(MergeArgs a) {
     if (mx != -INFINITY) {
         lse = mx + __logf(tot);
         const float inv = 1.f / tot;
-        r.x *= inv;
-        r.y *= inv;
-        r.z *= inv;
-        r.w *= inv;
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+            r[hh].x *= inv;
+            r[hh].y *= inv;
+            r[hh].z *= inv;
+            r[hh].w *= inv;
+        }
     }
     const int b = bh / a.g.H, h = bh % a.g.H;
     __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.g.sb + (int64_t)h * a.g.sh +
                        (int64_t)t * a.g.st;
-    if (d < D) *reinterpret_cast<uint2*>(O + d) = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        const int d = 4 * lane + 128 * hh;
+        if (d < D)
+            *reinterpret_cast<uint2*>(O + d) = make_uint2(pack_bf16(r[hh].x, r[hh].y), pack_bf16(r[hh].z, r[hh].w));
+    }
     if (lane == 0) a.lse[(int64_t)bh * a.g.T + t] = lse;
 }
 
@@ -154,7 +176,10 @@ cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s) {
     if (a.total_work <= 0) return cudaSuccess;
     const int64_t blocks = (a.total_work + 7) / 8;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    merge_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+    if (a.g.D > 128)
+        merge_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else
+        merge_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

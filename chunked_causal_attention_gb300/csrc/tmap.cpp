@@ -23,9 +23,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 // Rank-4 map of a [B, T, H, D]-strided tensor (axes 1..3 sorted by stride),
-// box = box_cols elements of the head dim x 128 tokens, 128-byte swizzle.
+// box = box_cols elements of the head dim x box_rows tokens, 128-byte swizzle.
 static bool make_map4(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, CUtensorMapDataType dt,
-                      int elem_bytes, int box_cols) {
+                      int elem_bytes, int box_cols, int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
     struct Ax {
@@ -47,7 +47,7 @@ static bool make_map4(CUtensorMap* m, const void* base, const Geom& g, TcMaps& m
         dims[i + 1] = (cuuint64_t)ax[i].dim;
         strides[i] = (cuuint64_t)ax[i].stride * (cuuint64_t)elem_bytes;
         if (ax[i].which == 0) {
-            box[i + 1] = 128;
+            box[i + 1] = (cuuint32_t)box_rows;
             mp.pos_t = i + 1;
         } else if (ax[i].which == 1) {
             mp.pos_h = i + 1;
@@ -60,12 +60,12 @@ static bool make_map4(CUtensorMap* m, const void* base, const Geom& g, TcMaps& m
     return r == CUDA_SUCCESS;
 }
 
-bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp) {
-    return make_map4(m, base, g, mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64);
+bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, int box_rows) {
+    return make_map4(m, base, g, mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, box_rows);
 }
 
 bool make_kv_acc_map(CUtensorMap* m, float* acc, const Geom& gkv, TcMaps& mp) {
-    return make_map4(m, acc, gkv, mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32);
+    return make_map4(m, acc, gkv, mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 128);
 }
 
 bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows) {

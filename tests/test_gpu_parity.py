@@ -234,6 +234,40 @@ def test_head_dims_between_tile_widths(D):
     full_check(q, k, v, do, P.plan_varlen(cu, 256, P.FLOPS_RESPLIT_EDGES), True, what=f"D{D} packed")
 
 
+@pytest.mark.parametrize("D", [136, 192, 256])
+def test_wide_head_dims_forward(D):
+    """Head dims above 128 (forward only) run on 256-wide tiles with 64-key K/V
+    tiles: dense rows with ragged tiles and an edge re-split (the merge path of
+    256-wide rows), P-part re-splits, packed documents and grouped key/value
+    heads, every row against the oracle. The backward refuses them on the host."""
+    q, k, v, do = (x.cuda() for x in make_inputs(2, 3, 1000, D, seed=190 + D))
+    full_check(q, k, v, do, P.plan(1000, 3, P.FLOPS_RESPLIT_EDGES), False, backward=False, what=f"D{D} dense")
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, 1500, D, seed=191 + D))
+    full_check(q, k, v, do, [(0, 700, 0, -4), (700, 1100, 0, -3), (1100, 1500, 0, 0)], False, backward=False,
+               what=f"D{D} P-part")
+    lens = [1, 63, 65, 127, 129, 300, 700]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, cu[-1], D, seed=195 + D, packed=True))
+    full_check(q, k, v, do, P.plan_varlen(cu, 256, P.FLOPS_RESPLIT_EDGES), True, backward=False,
+               what=f"D{D} packed")
+    # grouped key/value heads: 4 query heads on 2 key/value heads
+    L, H, Hkv = 640, 4, 2
+    q = make_inputs(1, H, L, D, seed=197 + D)[0].cuda()
+    k, v = (x.cuda() for x in make_inputs(1, Hkv, L, D, seed=198 + D)[1:3])
+    chunks = P.plan(L, 2, P.FLOPS)
+    o, lse = cca.forward(q, k, v, chunks)
+    torch.cuda.synchronize()
+    for h in range(H):
+        kh, vh = head(k, 0, h // 2, False), head(v, 0, h // 2, False)
+        ro, rl = A.forward(head(q, 0, h, False), kh, vh, default_scale(D))
+        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"D{D} grouped h{h}")
+    with pytest.raises(cca.AttnError) as e:
+        cca.backward(q, k, v, o, lse, torch.zeros_like(q), chunks)
+    assert e.value.status == 3
+
+
 def test_head_dim_padding_leaves_neighbours_untouched():
     """With D = 80 on the 128-wide tiles, the dims past D of a row are never
     written: rows of a wider buffer viewed with D = 80 keep their tail."""
