@@ -14,14 +14,16 @@ from ._lib import (AttnError, EXPORTS, PASS_BWD, PASS_BWD_CHUNK, PASS_FWD, PLAN_
                    PLAN_UNIFORM, attn_bwd, attn_bwd_chunk, attn_bwd_dq, attn_bwd_prep, attn_bwd_tiles, attn_fwd,
                    attn_fwd_merge, attn_fwd_noalloc, attn_fwd_tiles, attn_noalloc_status, attn_plan,
                    attn_plan_infinipipe, attn_plan_multiplex, attn_plan_varlen, attn_shape, attn_status,
-                   attn_workspace_size, lib, make_shape, shape_of, strerror, version)
+                   attn_workspace_size, lib, make_shape, shape_of, strerror, version,
+                   kernel_launches)
 
 __all__ = ["AttnError", "EXPORTS", "PLAN_UNIFORM", "PLAN_FLOPS", "PLAN_FLOPS_RESPLIT_EDGES", "attn_plan",
            "attn_plan_varlen", "attn_plan_infinipipe", "attn_plan_multiplex", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles", "attn_fwd_merge", "attn_bwd",
            "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq", "attn_bwd_chunk", "attn_fwd_noalloc",
            "attn_noalloc_status", "attn_status", "attn_shape",
            "make_shape", "shape_of", "workspace", "forward", "backward", "forward_streamed", "backward_streamed",
-           "PASS_FWD", "PASS_BWD", "PASS_BWD_CHUNK", "plan_infinipipe", "lib", "strerror", "version"]
+           "PASS_FWD", "PASS_BWD", "PASS_BWD_CHUNK", "plan_infinipipe", "lib", "strerror", "version",
+           "kernel_launches"]
 
 
 def workspace(shape: attn_shape, chunks: Sequence, pass_: int, device="cuda", per_chunk: bool = False):

@@ -28,7 +28,7 @@ PLAN_FLOPS_RESPLIT_EDGES = 2
 EXPORTS = ("attn_plan", "attn_plan_varlen", "attn_plan_multiplex", "attn_plan_infinipipe", "attn_workspace_size", "attn_fwd", "attn_fwd_tiles",
            "attn_fwd_merge", "attn_bwd", "attn_bwd_prep", "attn_bwd_tiles", "attn_bwd_dq",
            "attn_bwd_chunk", "attn_fwd_noalloc", "attn_noalloc_status", "attn_status", "attn_strerror",
-           "attn_version")
+           "attn_version", "attn_kernel_launches")
 
 # attn_workspace_size passes
 PASS_FWD = 0
@@ -88,6 +88,7 @@ _SIG = {
     "attn_status": ([_VP, _VP], ctypes.c_int),
     "attn_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "attn_version": ([], ctypes.c_char_p),
+    "attn_kernel_launches": ([], ctypes.c_uint64),
 }
 
 
@@ -113,6 +114,11 @@ def strerror(status: int) -> str:
 
 def version() -> str:
     return lib().attn_version().decode()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(lib().attn_kernel_launches())
 
 
 def _check(fn: str, st: int) -> None:

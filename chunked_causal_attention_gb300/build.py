@@ -20,7 +20,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_plan.cpp", "attn_api.cpp", "tmap.cpp", "fwd_tc.cu", "bwd_tc.cu", "merge.cu", "bwd_aux.cu", "noalloc.cu"]
+SOURCES = ["attn_plan.cpp", "attn_api.cpp", "tmap.cpp", "fwd_tc.cu", "bwd_tc.cu", "merge.cu", "bwd_aux.cu", "noalloc.cu",
+           "upload.cu"]
 
 
 def nvcc() -> str:

@@ -228,6 +228,8 @@ int check_chunks_stream(const attn_chunk* c, int32_t n, int32_t T) {
 
 }  // namespace
 
+std::atomic<uint64_t> attn::g_kernel_launches{0};
+
 void attn::wait_settings(uint64_t* wait_ns, int32_t* stall) {
     *wait_ns = 4000000000ull;
     *stall = 0;
@@ -245,9 +247,11 @@ bool attn::test_inconsistent_item() {
 
 namespace {
 
+// Host arrays (work lists, segments) to the workspace, as kernel parameters
+// (launch_upload): nothing refers to host memory once the call returns.
 int upload(void* dst, const void* src, size_t bytes, cudaStream_t s) {
     if (!bytes) return ATTN_OK;
-    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess ? ATTN_OK : ATTN_E_CUDA;
+    return launch_upload(dst, src, bytes, s) == cudaSuccess ? ATTN_OK : ATTN_E_CUDA;
 }
 
 int reset_header(void* ws, cudaStream_t s) {
@@ -523,5 +527,7 @@ const char* attn_strerror(int st) {
 }
 
 const char* attn_version(void) { return "libattn 0.1 sm_103a"; }
+
+uint64_t attn_kernel_launches(void) { return attn::g_kernel_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -186,6 +187,18 @@ int device_sm_count();
 // Key-range boundaries cb = k_0 < ... < k_P = qe of a chunk re-split into P
 // parts of equal visible-pair count (kv_split = -P). False if they collapse.
 bool resplit_bounds(int32_t qb, int32_t qe, int32_t cb, int32_t P, std::vector<int32_t>& k);
+
+// Kernels this library has enqueued since it was loaded (attn_kernel_launches);
+// every launcher passes its launch error through counted().
+extern std::atomic<uint64_t> g_kernel_launches;
+inline cudaError_t counted(cudaError_t e) {
+    if (e == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
+
+// Copy `bytes` of host data to device memory at dst (16-byte aligned), stream
+// ordered, as the parameters of one small kernel per 31 KB (upload.cu).
+cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t s);
 
 // Kernel launchers (return the launch error).
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s);   // fwd_tc.cu

@@ -85,7 +85,7 @@ cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
@@ -93,7 +93,7 @@ cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
     dq_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 }  // namespace attn

@@ -122,17 +122,19 @@ __device__ __forceinline__ void sg_block(uint32_t tm, int grp, int krow, int key
             tmem_ld16(tm + kColS + ncol, sr[b ^ 1]);
             tmem_ld16(tm + kColDP + ncol, dr[b ^ 1]);
         }
-        const float4* nl4 = reinterpret_cast<const float4*>(s_nl + col);
-        const float4* nd4 = reinterpret_cast<const float4*>(s_nd + col);
+        // this half-chunk's 16 values of -LSE*log2e (lanes 0-15) and of -D (lanes
+        // 16-31), one per lane from one load per warp, then to every lane by shuffles
+        const int ln = threadIdx.x & 31;
+        const float mine = ln < 16 ? s_nl[col + ln] : s_nd[col + ln - 16];
         uint32_t pp[8], dd[8];
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 L4 = nl4[e4], D4 = nd4[e4];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int e = 4 * e4 + 2 * u;
-                const float2 nl = u ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y);
-                const float2 nd = u ? make_float2(D4.z, D4.w) : make_float2(D4.x, D4.y);
+                const float2 nl = make_float2(__shfl_sync(0xffffffffu, mine, e), __shfl_sync(0xffffffffu, mine, e + 1));
+                const float2 nd = make_float2(__shfl_sync(0xffffffffu, mine, 16 + e),
+                                              __shfl_sync(0xffffffffu, mine, 17 + e));
                 const float2 x = ffma2(make_float2(__uint_as_float(sr[b][e]), __uint_as_float(sr[b][e + 1])), sl2x2, nl);
                 float p0 = ex2(x.x), p1 = ex2(x.y);
                 if (EDGE) {
@@ -694,7 +696,7 @@ cudaError_t launch_d(const BwdArgs& a, cudaStream_t s) {
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
     bwd_tc_kernel<D, GROUPED, PAD, ACC><<<grid, BT_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, am, a, mp, mpkv,
                                                                         (int32_t)work);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 // Head dims up to 64 run on 64-wide tiles, the others on 128-wide tiles.

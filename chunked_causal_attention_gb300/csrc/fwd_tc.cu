@@ -480,7 +480,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
     fwd_tc_kernel<D><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, mpkv, (int32_t)work);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 }  // namespace

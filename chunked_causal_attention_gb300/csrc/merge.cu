@@ -40,7 +40,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ballot; then lane p reads part p's LSE while every lane reads its slice of
 // the first two parts' O; the weights reach all lanes by shuffles.
 template <int NH>
-__global__ void __launch_bounds__(256, NH == 1 ? 5 : 4) merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(256, NH == 1 ? 5 : 3) merge_kernel(MergeArgs a) {
     const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= a.total_work) return;   // the same w for every lane of a warp
@@ -180,7 +180,7 @@ cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s) {
         merge_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(a);
     else
         merge_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 }  // namespace attn

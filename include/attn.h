@@ -48,10 +48,10 @@
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Compute calls only enqueue work and return before it completes.
  *   - chunks: a HOST array read during the call only. Each compute call lays
- *     out its work list on the host and copies it into the workspace with
- *     cudaMemcpyAsync on `stream` from host memory that is released when the
- *     call returns, so the calls are not meant for CUDA graph stream capture:
- *     a replayed copy would read released memory.
+ *     out its work list on the host and writes it into the workspace with
+ *     small copy kernels on `stream` that carry it in their launch
+ *     parameters (up to 31 KB per launch), so nothing on the device refers to
+ *     host memory after the call returns.
  *   - Every call returns an attn status code. Argument errors are detected on
  *     the host before anything is enqueued. Device-side errors are recorded in
  *     the workspace and read with attn_status(): ATTN_E_TIMEOUT (a bounded
@@ -333,6 +333,12 @@ const char* attn_strerror(int status);
 
 /* Library version string, e.g. "libattn 0.1 sm_103a". */
 const char* attn_version(void);
+
+/* Number of kernels this library has enqueued, on any stream and device,
+ * since it was loaded (a relaxed atomic counter; thread-safe). A compute
+ * call enqueues its tile kernels plus one small copy kernel per 31 KB of
+ * work list it writes into the workspace. No counterpart on the pages. */
+uint64_t attn_kernel_launches(void);
 
 #ifdef __cplusplus
 }

@@ -153,6 +153,7 @@ def test_grouped_heads_shape_validation():
 def test_compute_calls_reject_bad_arguments_on_host():
     """Validation happens before any CUDA call, so these run without a GPU."""
     L = cca.lib()
+    launches0 = cca.kernel_launches()
     ch, n = _lib.chunk_array(cca.attn_plan(1024, 4, 0))
     s = shape()
     fake = ctypes.c_void_p(4096)
@@ -181,6 +182,7 @@ def test_compute_calls_reject_bad_arguments_on_host():
     assert L.attn_fwd(fake, fake, fake, bad, nb, ctypes.byref(s), fake, fake, ws, 1 << 30, None) == 1
     assert L.attn_status(None, None) == 1
     assert cca.strerror(4).startswith("workspace")
+    assert cca.kernel_launches() == launches0   # a call refused on the host enqueues nothing
 
 
 def test_chunk_backward_workspace_and_host_errors():

@@ -201,6 +201,7 @@ def test_gpu_arm_json_line_with_a_fake_device(monkeypatch, capsys):
                  "attn_bwd", "attn_bwd_chunk"):
         monkeypatch.setattr(cca, name, lambda *a, _n=name: calls.append(_n))
     monkeypatch.setattr(cca, "attn_status", lambda *a: 0)
+    monkeypatch.setattr(cca, "kernel_launches", lambda: len(calls))   # one launch per stand-in call
     monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)
     monkeypatch.setitem(sys.modules, "torch", TorchProxy())
     monkeypatch.setitem(W.WORKLOADS, "mini_resplit",

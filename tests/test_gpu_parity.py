@@ -143,6 +143,39 @@ def test_stage_entry_points_equal_composed_calls():
     assert cca.attn_status(ws) == 0 and cca.attn_status(wsb) == 0
 
 
+def test_kernel_launch_count_per_call():
+    """Each stage call enqueues its kernel plus one copy kernel per 31 KB of work
+    list it writes into the workspace, and the library counts exactly those."""
+    L, H, D = 2000, 2, 128
+    q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=44))
+    chunks = P.plan(L, 3, P.FLOPS_RESPLIT_EDGES)
+    assert any(c[3] for c in chunks)
+    shape = cca.shape_of(q)
+    o, lse = torch.empty_like(q), torch.empty((1, H, L), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws, wsb = cca.workspace(shape, chunks, 0), cca.workspace(shape, chunks, 1)
+
+    def delta(fn):
+        n0 = cca.kernel_launches()
+        fn()
+        return cca.kernel_launches() - n0
+
+    assert delta(lambda: cca.attn_fwd_tiles(q, k, v, chunks, shape, o, lse, ws)) == 2       # items + tiles
+    assert delta(lambda: cca.attn_fwd_merge(chunks, shape, o, lse, ws)) == 3                # segs, bounds + merge
+    assert delta(lambda: cca.attn_bwd_prep(o, do, chunks, shape, wsb)) == 2                 # rows + prep
+    assert delta(lambda: cca.attn_bwd_tiles(q, k, v, lse, do, chunks, shape, dk, dv, wsb)) == 2
+    assert delta(lambda: cca.attn_bwd_dq(chunks, shape, dq, wsb)) == 2
+    # 1024 forward items of 32 bytes: the work list takes two copy kernels
+    T = 131072
+    q1, k1, v1, _ = (x.cuda() for x in make_inputs(1, 1, T, 64, seed=45))
+    ch = P.plan(T, 1, P.UNIFORM)
+    sh = cca.shape_of(q1)
+    o1, l1 = torch.empty_like(q1), torch.empty((1, 1, T), dtype=torch.float32, device="cuda")
+    assert delta(lambda: cca.attn_fwd_tiles(q1, k1, v1, ch, sh, o1, l1, cca.workspace(sh, ch, 0))) == 3
+    torch.cuda.synchronize()
+    assert cca.attn_status(ws) == 0 and cca.attn_status(wsb) == 0
+
+
 def test_backward_independent_of_chunk_cuts():
     L, H, D = 1500, 2, 64
     q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=55))
