@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_plan.cpp", "attn_api.cpp", "tmap.cpp", "fwd_tc.cu", "bwd_tc.cu", "merge.cu", "bwd_aux.cu", "noalloc.cu",
-           "upload.cu"]
+           "upload.cu", "bwd_wide.cu"]
 
 
 def nvcc() -> str:

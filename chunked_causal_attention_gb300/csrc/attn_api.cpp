@@ -18,10 +18,10 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Head dims: the forward takes any multiple of 8 up to 256, the backward up to
-// 128 (its dK and dV accumulators of a 256-wide tile would fill TMEM alone).
+// Head dims: any multiple of 8 up to 256, forward and backward (the backward
+// above 128 dims splits each key tile's outputs over two work items).
 constexpr int64_t kMaxDimFwd = 256;
-constexpr int64_t kMaxDimBwd = 128;
+constexpr int64_t kMaxDimBwd = 256;
 
 int check_shape(const attn_shape* s, Geom* g) {
     if (!s) return ATTN_E_INVAL;
@@ -373,7 +373,7 @@ int bwd_launch(const Geom& g, const BwdLayout& L, const void* q, const void* k, 
         a.group = kGroupBwd;
         wait_settings(&a.wait_ns, &a.stall);
         a.g = g;
-        if ((st = launched(launch_bwd_tiles_tc(a, s)))) return st;
+        if ((st = launched(g.D > 128 ? launch_bwd_tiles_wide(a, s) : launch_bwd_tiles_tc(a, s)))) return st;
     }
     if (stages & kDq) {
         DqArgs a{dq_acc, dq, segs, n_segs, L.rows, (uint32_t*)ws, g};

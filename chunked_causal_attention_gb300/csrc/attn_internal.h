@@ -175,8 +175,8 @@ struct TcMaps {
 // (128 bytes, 128-byte swizzle) x box_rows tokens. Fills `mp`. False on failure.
 bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, int box_rows = 128);
 // Rank-3 TMA map of the fp32 dQ accumulator [B*H][rows][D]: box of 32 floats
-// (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
-bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);
+// (128 bytes, 128-byte swizzle) x box_rows tokens, used for reduce-adds.
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows, int box_rows = 128);
 // Rank-4 TMA map of an fp32 dK or dV accumulator with the key/value strides of
 // gkv (element offsets of dk/dv): box of 32 floats (128 bytes, 128-byte
 // swizzle) x 128 tokens, used for reduce-adds. Fills `mp` (same axis order as
@@ -204,7 +204,8 @@ cudaError_t launch_upload(void* dst, const void* src, size_t bytes, cudaStream_t
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s);   // fwd_tc.cu
 cudaError_t launch_fwd_merge(const MergeArgs& a, cudaStream_t s);     // merge.cu
 cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);       // bwd_aux.cu
-cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s);   // bwd_tc.cu
+cudaError_t launch_bwd_tiles_tc(const BwdArgs& a, cudaStream_t s);   // bwd_tc.cu (head dims up to 128)
+cudaError_t launch_bwd_tiles_wide(const BwdArgs& a, cudaStream_t s); // bwd_wide.cu (129..256)
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);           // bwd_aux.cu
 
 }  // namespace attn

@@ -32,13 +32,15 @@
  *     strides for all eight tensors. Dense [B, H, L, D]: sb = H*L*D, sh = L*D,
  *     st = D. Packed [T, H, D] (B = 1): st = H*D, sh = D.
  *     Base pointers must be 16-byte aligned and sb, st, sh multiples of 8.
- *   - Head dim D: any multiple of 8 from 8 to 256 for the forward, from 8 to
- *     128 for the backward (attn_bwd*, attn_workspace_size passes 1 and 2
- *     return ATTN_E_UNSUPPORTED above 128). The tile kernels work on 64
+ *   - Head dim D: any multiple of 8 from 8 to 256 (InfiniPipe §III-A2 Eq. (3)
+ *     carries D and D_kv as model dimensions). The tile kernels work on 64
  *     (D <= 64), 128 (D <= 128) or 256 dims; the dims past D are loaded as
  *     zeros, which leaves every score, output and gradient unchanged, and are
  *     never written. Throughput in FLOP of the true D is therefore D/64,
- *     D/128 or D/256 of that at the tile width.
+ *     D/128 or D/256 of that at the tile width. Above 128 dims the backward
+ *     splits each 128-key tile into two work items, one per 128 output dims,
+ *     which both compute the tile's scores and score gradients: it does 7/5
+ *     of the backward's tensor work.
  *   - Grouped key/value heads (GQA/MQA): with Hkv > 0 in the shape, k, v, dk,
  *     dv (and the fp32 accumulators of attn_bwd_chunk) have Hkv heads and
  *     their own strides sb_kv, st_kv, sh_kv; query head h reads key/value head
@@ -74,7 +76,7 @@ extern "C" {
 #define ATTN_OK             0
 #define ATTN_E_INVAL        1  /* bad shape, chunk table, mode or pointer      */
 #define ATTN_E_ALIGN        2  /* pointer or stride not 16-byte aligned        */
-#define ATTN_E_UNSUPPORTED  3  /* head dim not a multiple of 8 in [8, 256] (backward: [8, 128]) */
+#define ATTN_E_UNSUPPORTED  3  /* head dim not a multiple of 8 in [8, 256] */
 #define ATTN_E_WORKSPACE    4  /* workspace NULL or smaller than required      */
 #define ATTN_E_CUDA         5  /* a CUDA runtime call or kernel launch failed  */
 #define ATTN_E_TIMEOUT      6  /* device: a bounded wait gave up               */
@@ -104,8 +106,7 @@ typedef struct {
 
 typedef struct {
     int64_t B, H, T, D;   /* batch rows, heads, tokens per row, head dim
-                             (a multiple of 8, 8 <= D <= 256; the backward
-                             takes D <= 128)                                 */
+                             (a multiple of 8, 8 <= D <= 256)               */
     int64_t sb, st, sh;   /* element strides of batch, token, head           */
     float   scale;        /* softmax scale; usually 1/sqrt(D)                */
     int64_t Hkv;          /* key/value heads (H % Hkv == 0); 0: Hkv = H     */

@@ -94,19 +94,16 @@ def test_workspace_size_validation():
     ch = cca.attn_plan(1024, 4, 0)
     assert cca.attn_workspace_size(shape(), ch, 0) >= 256
     assert cca.attn_workspace_size(shape(), ch, 1) >= 2 * 1024 * 64 * 4
-    # head dims: multiples of 8 from 8 to 128 both ways, and up to 256 forward only
-    for D in (8, 40, 80, 96, 120):
-        assert cca.attn_workspace_size(shape(D=D), ch, 1) >= 2 * 1024 * D * 4
-    for D in (136, 192, 256):
+    # head dims: multiples of 8 from 8 to 256, forward and backward
+    for D in (8, 40, 80, 96, 120, 136, 192, 256):
         assert cca.attn_workspace_size(shape(D=D), ch, 0) >= 256
-        for pass_ in (1, 2):
-            with pytest.raises(cca.AttnError) as e:
-                cca.attn_workspace_size(shape(D=D), ch if pass_ == 1 else ch[:1], pass_)
-            assert e.value.status == 3                          # the backward stops at 128
+        assert cca.attn_workspace_size(shape(D=D), ch, 1) >= 2 * 1024 * D * 4
+        assert cca.attn_workspace_size(shape(D=D), ch[:1], 2) >= 256
     for D in (4, 100, 264, 512):
-        with pytest.raises(cca.AttnError) as e:
-            cca.attn_workspace_size(shape(D=D), ch, 0)
-        assert e.value.status == 3
+        for pass_ in (0, 1, 2):
+            with pytest.raises(cca.AttnError) as e:
+                cca.attn_workspace_size(shape(D=D), ch if pass_ < 2 else ch[:1], pass_)
+            assert e.value.status == 3
     bad = [(0, 600, 0, 0), (500, 1024, 0, 0)]                  # overlapping
     with pytest.raises(cca.AttnError):
         cca.attn_workspace_size(shape(), bad, 0)
@@ -158,12 +155,10 @@ def test_compute_calls_reject_bad_arguments_on_host():
     s = shape()
     fake = ctypes.c_void_p(4096)
     ws = ctypes.c_void_p(1 << 20)
-    # D unsupported (not a multiple of 8, or above 256; the backward above 128)
+    # D unsupported (not a multiple of 8, or above 256)
     for D in (100, 264):
         sD = cca.make_shape(1, 2, 1024, D, 2 * 1024 * D, D, 1024 * D, 0.1)
         assert L.attn_fwd(fake, fake, fake, ch, n, ctypes.byref(sD), fake, fake, ws, 1 << 30, None) == 3
-    for D in (136, 256):
-        sD = cca.make_shape(1, 2, 1024, D, 2 * 1024 * D, D, 1024 * D, 0.1)
         assert L.attn_bwd(fake, fake, fake, fake, fake, fake, ch, n, ctypes.byref(sD), fake, fake, fake, ws,
                           1 << 30, None) == 3
         one, n1 = _lib.chunk_array(cca.attn_plan(1024, 4, 0)[:1])

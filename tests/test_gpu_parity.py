@@ -268,37 +268,59 @@ def test_head_dims_between_tile_widths(D):
 
 
 @pytest.mark.parametrize("D", [136, 192, 256])
-def test_wide_head_dims_forward(D):
-    """Head dims above 128 (forward only) run on 256-wide tiles with 64-key K/V
-    tiles: dense rows with ragged tiles and an edge re-split (the merge path of
-    256-wide rows), P-part re-splits, packed documents and grouped key/value
-    heads, every row against the oracle. The backward refuses them on the host."""
+def test_wide_head_dims(D):
+    """Head dims above 128 run on 256-wide tiles: the forward with 64-key K/V
+    tiles, the backward with each 128-key tile split into two work items by
+    output dims and 64-query blocks. Dense rows with ragged tiles and an edge
+    re-split (the merge path of 256-wide rows), P-part re-splits, packed
+    documents with one-token and off-grid documents, grouped key/value heads
+    and chunk-streamed calls (fp32 dK/dV accumulators), every row and key
+    against the oracle."""
     q, k, v, do = (x.cuda() for x in make_inputs(2, 3, 1000, D, seed=190 + D))
-    full_check(q, k, v, do, P.plan(1000, 3, P.FLOPS_RESPLIT_EDGES), False, backward=False, what=f"D{D} dense")
+    full_check(q, k, v, do, P.plan(1000, 3, P.FLOPS_RESPLIT_EDGES), False, what=f"D{D} dense")
     q, k, v, do = (x.cuda() for x in make_inputs(1, 2, 1500, D, seed=191 + D))
-    full_check(q, k, v, do, [(0, 700, 0, -4), (700, 1100, 0, -3), (1100, 1500, 0, 0)], False, backward=False,
-               what=f"D{D} P-part")
+    full_check(q, k, v, do, [(0, 700, 0, -4), (700, 1100, 0, -3), (1100, 1500, 0, 0)], False, what=f"D{D} P-part")
     lens = [1, 63, 65, 127, 129, 300, 700]
     cu = [0]
     for n in lens:
         cu.append(cu[-1] + n)
     q, k, v, do = (x.cuda() for x in make_inputs(1, 2, cu[-1], D, seed=195 + D, packed=True))
-    full_check(q, k, v, do, P.plan_varlen(cu, 256, P.FLOPS_RESPLIT_EDGES), True, backward=False,
-               what=f"D{D} packed")
-    # grouped key/value heads: 4 query heads on 2 key/value heads
+    full_check(q, k, v, do, P.plan_varlen(cu, 256, P.FLOPS_RESPLIT_EDGES), True, what=f"D{D} packed")
+    # grouped key/value heads: 4 query heads on 2 key/value heads; dK/dV of a
+    # key/value head sum over its query heads
     L, H, Hkv = 640, 4, 2
-    q = make_inputs(1, H, L, D, seed=197 + D)[0].cuda()
+    q, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=197 + D)[0:4:3])
     k, v = (x.cuda() for x in make_inputs(1, Hkv, L, D, seed=198 + D)[1:3])
     chunks = P.plan(L, 2, P.FLOPS)
     o, lse = cca.forward(q, k, v, chunks)
+    dq, dk, dv = cca.backward(q, k, v, o, lse, do, chunks)
     torch.cuda.synchronize()
-    for h in range(H):
-        kh, vh = head(k, 0, h // 2, False), head(v, 0, h // 2, False)
-        ro, rl = A.forward(head(q, 0, h, False), kh, vh, default_scale(D))
-        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"D{D} grouped h{h}")
-    with pytest.raises(cca.AttnError) as e:
-        cca.backward(q, k, v, o, lse, torch.zeros_like(q), chunks)
-    assert e.value.status == 3
+    sc = default_scale(D)
+    for hk in range(Hkv):
+        hs = range(2 * hk, 2 * hk + 2)
+        rdqs, rdk, rdv, ros, rls = A.grouped_backward([head(q, 0, h, False) for h in hs], head(k, 0, hk, False),
+                                                      head(v, 0, hk, False), [head(do, 0, h, False) for h in hs],
+                                                      sc, None)
+        for g, h in enumerate(hs):
+            check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ros[g], rls[g], f"D{D} grouped h{h}")
+            check_grad(head(dq, 0, h, False), rdqs[g], f"D{D} grouped dQ h{h}")
+        check_grad(head(dk, 0, hk, False), rdk, f"D{D} grouped dK hk{hk}")
+        check_grad(head(dv, 0, hk, False), rdv, f"D{D} grouped dV hk{hk}")
+    # chunk-streamed calls: forward per chunk, backward per chunk in reverse order
+    # with the fp32 accumulators; every key row is emitted from its accumulator
+    chunks = P.plan(1000, 4, P.FLOPS_RESPLIT_EDGES)
+    q, k, v, do = (x.cuda() for x in make_inputs(1, 2, 1000, D, seed=199 + D))
+    o, lse = cca.forward_streamed(q, k, v, chunks)
+    dq, dk, dv, dk_acc, dv_acc = cca.backward_streamed(q, k, v, o, lse, do, chunks)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, dk_acc.to(torch.bfloat16)) and torch.equal(dv, dv_acc.to(torch.bfloat16))
+    for h in range(2):
+        qh, kh, vh, doh = (head(x, 0, h, False) for x in (q, k, v, do))
+        rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, sc, None)
+        check_fwd(head(o, 0, h, False), lse_head(lse, 0, h), ro, rl, f"D{D} streamed h{h}")
+        check_grad(head(dq, 0, h, False), rdq, f"D{D} streamed dQ h{h}")
+        check_grad(head(dk, 0, h, False), rdk, f"D{D} streamed dK h{h}")
+        check_grad(head(dv, 0, h, False), rdv, f"D{D} streamed dV h{h}")
 
 
 def test_head_dim_padding_leaves_neighbours_untouched():
