@@ -19,8 +19,8 @@
 // Per query block, all 8 warps step together: one leader thread (warp 1,
 // lane 0) issues the TMA loads and the MMAs; every warp computes 32 queries x
 // 32 keys of the softmax gradient (TMEM lanes = keys) and drains 32 queries x
-// 32 dims of dQ^T (TMEM lanes = dims) into a staging tile in the Q buffer,
-// which the leader adds into the fp32 dQ accumulator with TMA reduce-adds.
+// 32 dims of dQ^T (TMEM lanes = dims) into the fp32 dQ accumulator by
+// reductions in L2 while the next block's Q and dO load.
 //   S^T  = K Q^T          M=128 keys, N=64 queries, K=256 dims   (SS, K-major)
 //   dP^T = V dO^T         as S^T
 //   dV_h += P^T dO_h      M=128 keys, N=128 dims,  K=64 queries  (A = P^T in TMEM, B MN-major)
@@ -46,7 +46,7 @@ struct WideLayout {
     static constexpr int QB_TILE = kQB * 256 * 2;   // 4 boxes of 64 rows x 64 dims (8 KB each)
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + KV_TILE;
-    static constexpr int Q_OFF = V_OFF + KV_TILE;   // also the dQ^T staging (4 x 64 rows x 32 fp32)
+    static constexpr int Q_OFF = V_OFF + KV_TILE;
     static constexpr int DO_OFF = Q_OFF + QB_TILE;
     static constexpr int DS_OFF = DO_OFF + QB_TILE; // dS^T: 128 keys x 64 queries bf16, 128-byte swizzle
     static constexpr int NL_OFF = DS_OFF + 16384;   // 64 floats: -LSE_t * log2 e
@@ -83,7 +83,7 @@ template <bool ACC>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     bwd_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                    const __grid_constant__ CUtensorMap tmdq, const BwdArgs a, const TcMaps mp, const TcMaps mpkv,
+                    const BwdArgs a, const TcMaps mp, const TcMaps mpkv,
                     const int32_t n_work) {
     using LY = WideLayout;
     extern __shared__ uint8_t smem_raw[];
@@ -183,10 +183,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     got_q += ok;
                 }
                 if (ok) {
-                    ok = mbar_wait(bar(LY::B_DO), got_do & 1, abort_flag, a.status, a.wait_ns);
-                    got_do += ok;
-                }
-                if (ok) {
+                    // S^T as soon as Q is in, dP^T once dO is
                     tc_fence_after();
                     const uint32_t k0 = sbase + LY::K_OFF, v0 = sbase + LY::V_OFF;
                     const uint32_t q0 = sbase + LY::Q_OFF, o0 = sbase + LY::DO_OFF;
@@ -197,14 +194,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                         mma_ss(tmem + cS, sdesc_sw128(k0 + ok_, 16, 1024), sdesc_sw128(q0 + oq, 16, 1024), id_s,
                                kk > 0);
                     }
+                    ok = mbar_wait(bar(LY::B_DO), got_do & 1, abort_flag, a.status, a.wait_ns);
+                    got_do += ok;
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const uint32_t ok_ = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t oq = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ss(tmem + cDP, sdesc_sw128(v0 + ok_, 16, 1024), sdesc_sw128(o0 + oq, 16, 1024), id_s,
-                               kk > 0);
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const uint32_t ok_ = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * 8192 + (kk & 3) * 32;
+                            mma_ss(tmem + cDP, sdesc_sw128(v0 + ok_, 16, 1024), sdesc_sw128(o0 + oq, 16, 1024),
+                                   id_s, kk > 0);
+                        }
+                        mma_commit(bar(LY::B_SDP));
                     }
-                    mma_commit(bar(LY::B_SDP));
                 }
             }
             tc_fence_before();
@@ -283,48 +285,30 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             }
             ok = mbar_wait_warp(bar(LY::B_G), ph_g & 1, abort_flag, a.status, a.wait_ns);
             ++ph_g;
-            // Q, dO and dS are free: the next block's dO goes out now, its Q once the
-            // dQ staging (in the Q buffer) has been read
+            // Q, dO and dS are free: the next block's Q and dO go out now
             if (leader && ok && !a.stall && n + 1 < nblk) {
+                mbar_expect_tx(bar(LY::B_Q), LY::QB_TILE);
+                load_wide(sbase + LY::Q_OFF, &tmq, bar(LY::B_Q), mp, blk_row(n + 1), blk_head(n + 1), b, 8192);
+                ++iss_q;
                 mbar_expect_tx(bar(LY::B_DO), LY::QB_TILE);
                 load_wide(sbase + LY::DO_OFF, &tmdo, bar(LY::B_DO), mp, blk_row(n + 1), blk_head(n + 1), b, 8192);
                 ++iss_do;
             }
+            // dQ^T: TMEM lane = dim 32*(warp&3) + lane of this half, columns = queries;
+            // added into the fp32 accumulator by reductions in L2, one 128-byte row
+            // segment (32 dims of one query) per warp instruction
             if (ok) {
-                // dQ^T: TMEM lane = dim 32*(warp&3) + lane of this half, columns = queries;
-                // staged as [query][dim] fp32 in 4 sub-tiles of 32 dims (128-byte swizzle)
                 tc_fence_after();
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_addr + cDQ + 32 * ch, r);
                 tmem_ld_wait();
-                uint8_t* sub = sm + LY::Q_OFF + (warp & 3) * 8192;
+                const int d = 128 * half + 32 * (warp & 3) + lane;
+                if (d < Dh) {
+                    float* dst = a.dq_acc + (bhq * a.rows + item.row_off + i0 + 32 * ch) * (int64_t)Dh + d;
+                    const int nrow = min(32, item.q_end - (i0 + 32 * ch));   // rows past the range add nothing
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int qr = 32 * ch + e;
-                    *reinterpret_cast<float*>(sub + qr * 128 + ((((lane >> 2) ^ (qr & 7))) << 4) + (lane & 3) * 4) =
-                        __uint_as_float(r[e]) * a.g.scale;
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            if (!__syncthreads_and(ok && !*abort_flag)) {
-                ok = false;
-                break;
-            }
-            if (leader) {
-                // boxes that start past the head dim hold only its zero dims; a box that
-                // runs past it is clipped by the TMA unit
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    if (128 * half + 32 * cc < Dh)
-                        tma_reduce_add_3d(&tmdq, sbase + LY::Q_OFF + cc * 8192, 128 * half + 32 * cc,
-                                          i0 + item.row_off, (int)bhq);
-                bulk_commit();
-                bulk_wait_read_all();
-                if (!a.stall && n + 1 < nblk) {
-                    mbar_expect_tx(bar(LY::B_Q), LY::QB_TILE);
-                    load_wide(sbase + LY::Q_OFF, &tmq, bar(LY::B_Q), mp, blk_row(n + 1), blk_head(n + 1), b, 8192);
-                    ++iss_q;
+                    for (int e = 0; e < 32; ++e)
+                        if (e < nrow) atomicAdd(dst + (int64_t)e * Dh, __uint_as_float(r[e]) * a.g.scale);
                 }
             }
         }
@@ -380,7 +364,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     // ---------------------------------------------------------------- teardown
     if (leader) {
         // loads that a wait which gave up left in flight land before the CTA leaves
-        // (bounded); then the reduce-adds complete
+        // (bounded)
         const uint64_t t0 = globaltimer();
         while (iss_kv > got_kv && !mbar_try_wait(bar(LY::B_KV), got_kv & 1) && globaltimer() - t0 < a.wait_ns) {
         }
@@ -388,7 +372,6 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         while (iss_do > got_do && !mbar_try_wait(bar(LY::B_DO), got_do & 1) && globaltimer() - t0 < a.wait_ns) {
         }
-        bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -411,12 +394,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 template <bool ACC>
 cudaError_t launch_wide(const BwdArgs& a, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mdo, mdq;
+    CUtensorMap mq, mk, mv, mdo;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
     const Geom gkv = a.g.kv();
     if (!make_tile_map(&mq, a.q, a.g, mp, kQB) || !make_tile_map(&mk, a.k, gkv, mpkv) ||
-        !make_tile_map(&mv, a.v, gkv, mpkv) || !make_tile_map(&mdo, a.dout, a.g, mp, kQB) ||
-        !make_dq_acc_map(&mdq, a.dq_acc, a.g, a.rows, kQB))
+        !make_tile_map(&mv, a.v, gkv, mpkv) || !make_tile_map(&mdo, a.dout, a.g, mp, kQB))
         return cudaErrorInvalidValue;
     const int64_t work = 2 * (int64_t)a.n_items * a.g.B * a.g.Hkv;   // two output halves per key tile
     if (work <= 0) return cudaSuccess;
@@ -425,7 +407,7 @@ cudaError_t launch_wide(const BwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(bwd_wide_kernel<ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    bwd_wide_kernel<ACC><<<grid, BW_THREADS, smem, s>>>(mq, mk, mv, mdo, mdq, a, mp, mpkv, (int32_t)work);
+    bwd_wide_kernel<ACC><<<grid, BW_THREADS, smem, s>>>(mq, mk, mv, mdo, a, mp, mpkv, (int32_t)work);
     return counted(cudaGetLastError());
 }
 

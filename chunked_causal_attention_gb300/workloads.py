@@ -20,6 +20,8 @@ no dataset is available here, so all tensors are i.i.d. N(0, 1) cast to bf16):
 * ``gqa_128k``   B=1 H=32 with 8 key/value heads (grouped-query attention,
                  4 query heads per key/value head), D=128 L=131072, the same
                  plan as 7b_128k.
+* ``d256_32k``   B=1 H=16 D=256 L=32768 (the 7B hidden size of 4096 as 16
+                 heads of 256 dims), FLOPS plan N=8 with the edges re-split.
 """
 from __future__ import annotations
 
@@ -95,6 +97,7 @@ WORKLOADS = {
                             max_chunk_tokens=16384, doc_lens=skewed_doc_lengths()),
     "13b_1m": Workload("13b_1m", 1, 40, 128, 1048576, N=64, mode=PLAN_FLOPS, seed=1238),
     "gqa_128k": Workload("gqa_128k", 1, 32, 128, 131072, N=16, mode=PLAN_FLOPS_RESPLIT_EDGES, seed=1239, Hkv=8),
+    "d256_32k": Workload("d256_32k", 1, 16, 256, 32768, N=8, mode=PLAN_FLOPS_RESPLIT_EDGES, seed=1240),
 }
 
 

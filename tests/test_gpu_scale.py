@@ -47,6 +47,24 @@ def test_7b_32k():
     assert cca.attn_status(cca.workspace(cca.shape_of(q), chunks, 0)) in (0,)
 
 
+def test_d256_32k():
+    """256-dim heads at 32K tokens (the split backward's items walk up to 512
+    query blocks): head 0 in full, sampled rows of the others, invariants."""
+    w = WORKLOADS["d256_32k"]
+    q, k, v, do = (x.cuda() for x in workload_inputs(w))
+    chunks = plan_of(w)
+    assert chunks == P.plan(w.L, w.N, w.mode)
+    o, lse, dq, dk, dv = run_gpu(q, k, v, do, chunks)
+    qh, kh, vh, doh = (head(x, 0, 0, False) for x in (q, k, v, do))
+    rdq, rdk, rdv, ro, rl = A.backward(qh, kh, vh, doh, w.scale, None, row_block=1024)
+    check_fwd(head(o, 0, 0, False), lse_head(lse, 0, 0), ro, rl, "d256 h0")
+    check_grad(head(dq, 0, 0, False), rdq, "d256 dQ h0")
+    check_grad(head(dk, 0, 0, False), rdk, "d256 dK h0")
+    check_grad(head(dv, 0, 0, False), rdv, "d256 dV h0")
+    sampled_rows_check(w, q, k, v, do, o, lse, dq, 512, 7, "d256")
+    invariants_check(w, q, do, dk, dv, "d256")
+
+
 def test_7b_128k():
     w = WORKLOADS["7b_128k"]
     q, k, v, do = (x.cuda() for x in workload_inputs(w))
