@@ -129,7 +129,8 @@ void fwd_layout(const Geom& g, const attn_chunk* c, int32_t n, FwdLayout& L) {
             MergeSeg s;
             s.row0 = pr0; s.R = R; s.P = P; s.kb = (int32_t)L.kbounds.size();
             s.off0 = off0; s.blk = blk; s.work0 = L.merge_work;
-            L.merge_work += (int64_t)R * BH;
+            const int64_t rb = merge_rows_per_block(g.D);
+            L.merge_work += ((int64_t)R * BH + rb - 1) / rb;
             L.segs.push_back(s);
             L.kbounds.insert(L.kbounds.end(), k.begin(), k.end());
         }
@@ -321,6 +322,10 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
         a.status = (uint32_t*)ws;
         a.n_segs = (int32_t)L.segs.size();
         a.total_work = L.merge_work;
+        for (int32_t i = 0; i < (int32_t)L.segs.size() && i < kMergeSegsInline; ++i) a.segs_inline[i] = L.segs[i];
+        a.bulk_parts = 2;
+        for (const MergeSeg& sg : L.segs)
+            if (sg.P <= kBulkParts) a.bulk_parts = std::max(a.bulk_parts, sg.P);
         a.g = g;
         if ((st = launched(launch_fwd_merge(a, s)))) return st;
     }

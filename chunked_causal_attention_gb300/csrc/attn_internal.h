@@ -42,7 +42,7 @@ struct MergeSeg {
     int32_t row0, R;
     int32_t P, kb;
     int64_t off0, blk;
-    int64_t work0;        // first work index of this segment (rows * BH prefix)
+    int64_t work0;        // first merge block of this segment (blocks of merge_rows_per_block rows)
 };
 static_assert(sizeof(MergeSeg) == 40, "MergeSeg layout");
 
@@ -102,6 +102,11 @@ struct FwdArgs {
     Geom g;
 };
 
+// Segment tables up to this length travel in the merge kernel's parameters.
+constexpr int kMergeSegsInline = 8;
+// Segments of up to this many parts are merged from bulk copies in shared memory.
+constexpr int kBulkParts = 4;
+
 struct MergeArgs {
     void* o; float* lse;
     const float* ws_f;
@@ -111,9 +116,13 @@ struct MergeArgs {
     int32_t n_kbounds;
     uint32_t* status;
     int32_t n_segs;
-    int64_t total_work;   // sum over segments of R * B * H
+    int64_t total_work;   // merge blocks: sum over segments of ceil(R * B * H / merge_rows_per_block)
     Geom g;
+    MergeSeg segs_inline[kMergeSegsInline];   // a copy of segs when n_segs <= kMergeSegsInline
+    int32_t bulk_parts;   // segments of 2..bulk_parts parts take the bulk path (the largest such P, at least 2)
 };
+// Rows (of B*H*R per segment) that one block of the merge kernel takes.
+int merge_rows_per_block(int D);
 
 // delta and the dQ accumulator hold `rows` workspace rows per (batch, head):
 // delta[bh*rows + r], dq_acc[(bh*rows + r)*D + d]; segs map rows to tokens.
