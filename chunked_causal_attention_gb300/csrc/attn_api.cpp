@@ -305,6 +305,8 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_chunk* ch
             a.items = (const FwdItem*)(w + L.off_items);
             a.n_items = (int32_t)L.items.size();
             a.group = kGroupFwd;
+            a.max_kv = 0;
+            for (const FwdItem& it : L.items) a.max_kv = std::max(a.max_kv, it.kv_hi - it.kv_lo);
             wait_settings(&a.wait_ns, &a.stall);
             a.g = g;
             if ((st = launched(launch_fwd_tiles_tc(a, s)))) return st;

@@ -1,11 +1,12 @@
 // Forward tile kernel on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Persistent CTAs walk the cost-sorted work list (128 query rows x one key
-// range x one (batch, head)). The tiles are D = 64 or 128 dims wide; a head
-// dim below D loads its remaining dims as zeros (the TMA maps carry the true
-// head dim) and only its own dims are written. Warp roles:
+// range x one (batch, head)). The tiles are D = 64, 128 or 256 dims wide; a
+// head dim below D loads its remaining dims as zeros (the TMA maps carry the
+// true head dim) and only its own dims are written. Warp roles:
 //   warp 0      TMA producer: Q tile once per item; K and V tiles of 128 keys
-//               through two-stage rings (128-byte swizzled, 64-column boxes),
+//               (64 at D = 256) through two- or three-stage rings (128-byte
+//               swizzled, 64-column boxes),
 //               from the key/value head of the item's query head (grouped
 //               heads: h / (H / Hkv)).
 //   warp 1      MMA issuer (one thread) and TMEM owner:
@@ -42,21 +43,26 @@ namespace {
 using namespace tc;
 
 constexpr int TC_THREADS = 256;
-constexpr int KV_STAGES = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 // Keys per K/V tile: 128, or 64 for the 256-wide head dims, whose Q tile (64 KB)
-// and two-stage K and V rings (4 x 32 KB) then fit in shared memory, and whose
+// and two-stage K and V rings (4 x 32 KB) then fit in shared memory (a Q tile
+// and three-stage rings of 128-key tiles take 224 KB at D = 128), and whose
 // two S buffers (2 x 64 columns) and O (256 columns) fit in TMEM.
 template <int D>
 constexpr int kBlockN = D > 128 ? 64 : 128;
 
-template <int D>
+// KVS: stages of the K and V rings. Three (D <= 128) when a head's K and V fit
+// the L2 several times over, so the deeper ring hides more of the L2 latency;
+// two for long key ranges, whose K/V tiles the CTAs of a head group share in
+// L2 only while they stay close together, and for the 256-wide tiles.
+template <int D, int KVS>
 struct FwdTcLayout {
     static constexpr int BN = kBlockN<D>;
+    static constexpr int KV_STAGES = KVS;
     static constexpr int TILE_Q = 128 * D * 2;          // bytes of the 128-row bf16 Q tile
     static constexpr int TILE_KV = BN * D * 2;          // bytes of one BN-row bf16 K or V tile
     static constexpr int Q_OFF = 0;
@@ -93,12 +99,13 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
     for (int a = 0; a < D / 64; ++a) tma_load_4d(dst + a * ROWS * 128, map, bar, a * 64, c1, c2, c3);
 }
 
-template <int D>
+template <int D, int KVS>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdArgs a, const TcMaps mp, const TcMaps mpkv,
                   const int32_t n_work) {
-    using LY = FwdTcLayout<D>;
+    using LY = FwdTcLayout<D, KVS>;
+    constexpr int KV_STAGES = KVS;
     constexpr int BN = LY::BN;                  // keys per K/V tile and columns per S buffer
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 }
 
-template <int D>
+template <int D, int KVS>
 cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     CUtensorMap mq, mk, mv;
     TcMaps mp{1, 2, 3}, mpkv{1, 2, 3};
@@ -475,11 +482,13 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
     const int64_t work = (int64_t)a.n_items * a.g.B * a.g.H;
     if (work <= 0) return cudaSuccess;
     if (work > INT32_MAX) return cudaErrorInvalidValue;
-    const size_t smem = FwdTcLayout<D>::ALLOC;
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = FwdTcLayout<D, KVS>::ALLOC;
+    static_assert(FwdTcLayout<D, KVS>::ALLOC <= 232448, "shared memory of the forward tile kernel");
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_tc_kernel<D, KVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(work, device_sm_count());
-    fwd_tc_kernel<D><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, mpkv, (int32_t)work);
+    fwd_tc_kernel<D, KVS><<<grid, TC_THREADS, smem, s>>>(mq, mk, mv, a, mp, mpkv, (int32_t)work);
     return counted(cudaGetLastError());
 }
 
@@ -488,8 +497,13 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t s) {
 cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s) {
     // head dims up to 64 run on 64-wide tiles, up to 128 on 128-wide tiles, the
     // others (up to 256) on 256-wide tiles with 64-key K/V tiles
-    if (a.g.D > 128) return launch_d<256>(a, s);
-    return a.g.D > 64 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+    if (a.g.D > 128) return launch_d<256, 2>(a, s);
+    // a three-stage ring while one head's K and V over the longest key range take
+    // at most 64 MB (131072 keys at 128 dims): measured faster at 32K and 128K
+    // tokens, slower at 1M
+    const bool deep = (int64_t)a.max_kv * a.g.D * 4 <= (int64_t)64 << 20;
+    if (a.g.D > 64) return deep ? launch_d<128, 3>(a, s) : launch_d<128, 2>(a, s);
+    return deep ? launch_d<64, 3>(a, s) : launch_d<64, 2>(a, s);
 }
 
 }  // namespace attn
