@@ -348,9 +348,11 @@ def test_head_dim_padding_leaves_neighbours_untouched():
 
 
 def test_concurrent_calls_on_two_streams():
-    """The library keeps no mutable state between calls: two problems run at
-    the same time on two streams, each with its own workspace, give what
-    they give one after the other (O, LSE, dK, dV bit for bit; dQ, whose fp32
+    """The calls that take a caller workspace keep no state that changes a
+    result between calls (attn_fwd_noalloc shares one library-held scratch
+    area among its calls, as its header says): two problems run at the same
+    time on two streams, each with its own workspace, give what they give one
+    after the other (O, LSE, dK, dV bit for bit; dQ, whose fp32
     reduce-adds run in any order, within the tolerance)."""
     cases = [(1, 4, 3000, 128, P.plan(3000, 3, P.FLOPS_RESPLIT_EDGES), 401),
              (2, 3, 2000, 64, P.plan(2000, 2, P.FLOPS), 402)]

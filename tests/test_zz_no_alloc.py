@@ -14,7 +14,10 @@ reads that path's device error word. This file checks it through the C ABI:
 - once against the float64 oracle;
 - that a bounded wait that gives up is reported by attn_noalloc_status and
   that the read clears it;
-- that a request larger than the scratch is refused on the host.
+- that a request larger than the scratch is refused on the host;
+- that a call after the caller resets the device (cudaDeviceReset) finds the
+  scratch in the new context (a child process, with no framework holding
+  device memory across the reset).
 
 pytest collects this file last.
 """
@@ -135,3 +138,19 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
     q = torch.empty(16, dtype=torch.bfloat16, device="cuda")   # never read: refused on the host
     st = call_noalloc(q, q, q, chunks, shape, q, q)
     assert st == ATTN_E_WORKSPACE, cca.strerror(st)
+
+
+def test_noalloc_after_a_device_reset():
+    import glob
+    import os
+    import subprocess
+    import sys
+    libs = sorted(glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
+    if not libs:
+        pytest.skip("no CUDA runtime library to reset the device through")
+    child = os.path.join(os.path.dirname(os.path.abspath(__file__)), "noalloc_reset_child.py")
+    r = subprocess.run([sys.executable, child, libs[0]], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = dict(line.split(" ", 1) for line in r.stdout.splitlines() if " " in line)
+    assert lines["status"].split() == ["0", "0", "0", "0"], r.stdout
+    assert lines["equal"] == "1" and lines["finite"] == "1", r.stdout
