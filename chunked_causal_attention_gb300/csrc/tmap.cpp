@@ -83,8 +83,8 @@ bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows,
 
 int device_sm_count() {
     int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) return 152;
     return c;
 }
 
