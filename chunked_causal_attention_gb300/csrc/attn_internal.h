@@ -185,8 +185,8 @@ struct TcMaps {
 // (128 bytes, 128-byte swizzle) x box_rows tokens. Fills `mp`. False on failure.
 bool make_tile_map(CUtensorMap* m, const void* base, const Geom& g, TcMaps& mp, int box_rows = 128);
 // Rank-3 TMA map of the fp32 dQ accumulator [B*H][rows][D]: box of 32 floats
-// (128 bytes, 128-byte swizzle) x box_rows tokens, used for reduce-adds.
-bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows, int box_rows = 128);
+// (128 bytes, 128-byte swizzle) x 128 tokens, used for reduce-adds.
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows);
 // Rank-4 TMA map of an fp32 dK or dV accumulator with the key/value strides of
 // gkv (element offsets of dk/dv): box of 32 floats (128 bytes, 128-byte
 // swizzle) x 128 tokens, used for reduce-adds. Fills `mp` (same axis order as

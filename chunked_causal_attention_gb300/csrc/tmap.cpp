@@ -68,12 +68,12 @@ bool make_kv_acc_map(CUtensorMap* m, float* acc, const Geom& gkv, TcMaps& mp) {
     return make_map4(m, acc, gkv, mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 128);
 }
 
-bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows, int box_rows) {
+bool make_dq_acc_map(CUtensorMap* m, float* dq_acc, const Geom& g, int32_t rows) {
     auto enc = encode_fn();
     if (!enc || rows <= 0) return false;
     cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)rows, (cuuint64_t)g.B * (cuuint64_t)g.H};
     cuuint64_t strides[2] = {(cuuint64_t)g.D * 4, (cuuint64_t)rows * g.D * 4};
-    cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+    cuuint32_t box[3] = {32, 128, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
