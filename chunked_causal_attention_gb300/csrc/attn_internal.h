@@ -97,7 +97,6 @@ struct FwdArgs {
     const FwdItem* items;
     int32_t n_items;
     int32_t group;        // items per head group in the work order
-    int32_t max_kv;       // the longest key range of an item (picks the K/V ring depth)
     uint64_t wait_ns;     // limit of every mbarrier wait
     int32_t stall;        // test only: the TMA producer issues nothing
     Geom g;

@@ -55,10 +55,9 @@ constexpr float kRescaleThreshold = 8.0f;      // log2 units
 template <int D>
 constexpr int kBlockN = D > 128 ? 64 : 128;
 
-// KVS: stages of the K and V rings. Three (D <= 128) when a head's K and V fit
-// the L2 several times over, so the deeper ring hides more of the L2 latency;
-// two for long key ranges, whose K/V tiles the CTAs of a head group share in
-// L2 only while they stay close together, and for the 256-wide tiles.
+// KVS: stages of the K and V rings: three for tiles up to 128 dims (the deeper
+// ring hides more of the latency of K/V tiles from L2 or DRAM), two for the
+// 256-wide tiles, whose shared memory holds no third stage.
 template <int D, int KVS>
 struct FwdTcLayout {
     static constexpr int BN = kBlockN<D>;
@@ -498,12 +497,7 @@ cudaError_t launch_fwd_tiles_tc(const FwdArgs& a, cudaStream_t s) {
     // head dims up to 64 run on 64-wide tiles, up to 128 on 128-wide tiles, the
     // others (up to 256) on 256-wide tiles with 64-key K/V tiles
     if (a.g.D > 128) return launch_d<256, 2>(a, s);
-    // a three-stage ring while one head's K and V over the longest key range take
-    // at most 64 MB (131072 keys at 128 dims): measured faster at 32K and 128K
-    // tokens, slower at 1M
-    const bool deep = (int64_t)a.max_kv * a.g.D * 4 <= (int64_t)64 << 20;
-    if (a.g.D > 64) return deep ? launch_d<128, 3>(a, s) : launch_d<128, 2>(a, s);
-    return deep ? launch_d<64, 3>(a, s) : launch_d<64, 2>(a, s);
+    return a.g.D > 64 ? launch_d<128, 3>(a, s) : launch_d<64, 3>(a, s);
 }
 
 }  // namespace attn
