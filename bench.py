@@ -34,16 +34,28 @@ CPU_SAMPLE_TOKENS = 40960     # causal prefix of one head timed on the host core
 
 
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic_7b_128k.json")
-KERNEL_SOURCES = ["bwd_tc.cu", "attn_api.cpp", "device_common.cuh", "tc_common.cuh", "attn_internal.h"]
+KERNEL_SOURCES = ["bwd_tc.cu", "device_common.cuh", "tc_common.cuh"]
+# the parts of attn_api.cpp that set the backward's work list, order and launch
+API_SECTIONS = [("// --------------------------------------------------------------- backward layout", "\n}  // namespace"),
+                ("constexpr int32_t kGroupBwd", "\n"),
+                ("int bwd_launch(", "\nint bwd_common(")]
 
 
 def kernel_source_hash():
-    """SHA-256 over the sources that define the backward tile kernel and its work order."""
+    """SHA-256 over what sets the backward tile kernel's memory traffic: its
+    source and device headers, and the backward work-list layout, head-group
+    constant and launch code of attn_api.cpp."""
     import hashlib
     h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_causal_attention_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "chunked_causal_attention_gb300", "csrc", f), "rb") as fh:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(csrc, "attn_api.cpp")) as fh:
+        api = fh.read()
+    for start, end in API_SECTIONS:
+        i = api.index(start)
+        h.update(api[i:api.index(end, i + len(start))].encode())
     return h.hexdigest()
 
 
