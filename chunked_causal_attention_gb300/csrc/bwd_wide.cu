@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 }
             }
         }
-        if (!ok) break;
+        // a wait of the last block may have given up in some warps only: the CTA
+        // decides together whether to write the epilogue or to leave
+        tc_fence_before();
+        if (!__syncthreads_and(ok && !*abort_flag)) break;
         // epilogue: warps 0-3 write dK_h * scale, warps 4-7 dV_h, one key row per thread
         {
             const int64_t roff = (int64_t)b * a.g.sb_kv + (int64_t)hk * a.g.sh_kv + (int64_t)key * a.g.st_kv;

@@ -37,8 +37,10 @@ def built():
         build.build()
 
 
-def test_stalled_producer_times_out_and_context_survives(monkeypatch):
-    L, H, D = 2048, 2, 128
+@pytest.mark.parametrize("D", [128, 256])
+def test_stalled_producer_times_out_and_context_survives(monkeypatch, D):
+    """D = 256 runs the 256-wide forward and the backward split by output dims."""
+    L, H = 2048, 2
     q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=88))
     chunks = P.plan(L, 2, P.FLOPS)
     shape = cca.shape_of(q)
@@ -73,15 +75,18 @@ def test_stalled_producer_times_out_and_context_survives(monkeypatch):
 ATTN_E_BOUNDS = 7
 
 
-def test_inconsistent_work_item_is_reported_and_not_used(monkeypatch):
+@pytest.mark.parametrize("D", [128, 256])
+def test_inconsistent_work_item_is_reported_and_not_used(monkeypatch, D):
     """Device-side index checks. With the test-only switch the first work item
     of each tile kernel gets an empty row range (forward: r1 = r0; backward:
     q_end = q_lo), a descriptor that addresses nothing outside the buffers but
     does not fit the shape's rules. Every role of the kernel checks the item
     before forming an address from it, records ATTN_E_BOUNDS and stops. The
     item's output rows keep their sentinel values (nothing was written for
-    it), and the same CUDA context then runs a normal forward and backward."""
-    L, H, D = 2048, 2, 128
+    it), and the same CUDA context then runs a normal forward and backward.
+    D = 256 runs the 256-wide forward and the backward split by output dims,
+    where both work items of the key tile (its two halves of dims) stop."""
+    L, H = 2048, 2
     q, k, v, do = (x.cuda() for x in make_inputs(1, H, L, D, seed=89))
     chunks = P.plan(L, 2, P.FLOPS)
     shape = cca.shape_of(q)
@@ -99,7 +104,7 @@ def test_inconsistent_work_item_is_reported_and_not_used(monkeypatch):
     assert torch.isnan(o[0, 0, L - 128:].float()).all() and torch.isnan(lse[0, 0, L - 128:]).all()
     cca.attn_bwd(q, k, v, o_good, lse_good, do, chunks, shape, dq, dk, dv, ws_b)
     assert cca.attn_status(ws_b) == ATTN_E_BOUNDS
-    # the first backward item is the heaviest: key tile 0 of head 0
+    # the first backward item is the heaviest: key tile 0 of head 0 (all its dims)
     assert torch.isnan(dk[0, 0, :128].float()).all() and torch.isnan(dv[0, 0, :128].float()).all()
 
     monkeypatch.delenv("ATTN_TEST_INCONSISTENT_ITEM")
