@@ -51,6 +51,36 @@ def test_traffic_record_is_gated_by_source_hash(tmp_path, monkeypatch):
     assert bench.measured_traffic("7b_128k") is None
 
 
+def test_source_hash_follows_the_backward_kernel_only(tmp_path, monkeypatch):
+    """The traffic record's hash covers the backward tile kernel, its device
+    headers and the backward's layout, order and launch code in attn_api.cpp:
+    an edit there changes it, an edit of the forward kernel or of forward-only
+    host code does not."""
+    import shutil
+    src = os.path.join(ROOT, "chunked_causal_attention_gb300", "csrc")
+    dst = tmp_path / "chunked_causal_attention_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+
+    def edited(name, old, new):
+        path = dst / name
+        text = path.read_text()
+        assert old in text
+        path.write_text(text.replace(old, new, 1))
+        h = bench.kernel_source_hash()
+        path.write_text(text)
+        return h
+
+    assert edited("fwd_tc.cu", "namespace attn {", "namespace attn {\n") == h0
+    assert edited("attn_api.cpp", "constexpr int32_t kGroupFwd", "constexpr int32_t kGroupFwd ") == h0
+    assert edited("bwd_tc.cu", "namespace attn {", "namespace attn {\n") != h0
+    assert edited("attn_api.cpp", "constexpr int32_t kGroupBwd", "constexpr int32_t kGroupBwd ") != h0
+    assert edited("attn_api.cpp", "void bwd_layout(", "void  bwd_layout(") != h0
+    assert edited("attn_api.cpp", "        a.group = kGroupBwd;", "        a.group = kGroupBwd; ") != h0
+    assert bench.kernel_source_hash() == h0
+
+
 def test_committed_traffic_record_names_its_kernel_and_command():
     with open(os.path.join(ROOT, "profiles", "traffic_7b_128k.json")) as f:
         rec = json.load(f)
